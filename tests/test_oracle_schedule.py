@@ -1,0 +1,113 @@
+"""Pins for the greedy throughput scheduler in the CPU oracle (DSpark guide,
+scheduler section): brute force over every length vector when Theta is unimodal,
+the early stop at the first local maximum when it is not, the two SPS limits
+with closed-form answers, ties, the batch cap, and the fixed-point reading."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+
+def _theta(a, ell, sps):
+    R = a.shape[0]
+    tau = sum(1.0 + a[r, :ell[r]].sum() for r in range(R))
+    B = sum(1 + ell[r] for r in range(R))
+    return tau * sps[B - 1]
+
+
+def test_survival_products_are_left_to_right_products():
+    c = np.array([[0.5, 0.5, 1.0, 0.25]], dtype=np.float32)
+    a = oracle.survival_products(c)
+    assert list(a[0]) == [0.5, 0.25, 0.25, 0.0625]
+    c = synth.confidences(51, 10, 7)
+    a = oracle.survival_products(c)
+    assert (np.diff(a, axis=1) <= 0).all()       # non-increasing in j
+
+
+def test_constant_sps_takes_everything():
+    c = synth.confidences(52, 6, 5)
+    res = oracle.schedule(c, np.full(64, 7.0))
+    assert (res.lengths == 5).all() and res.n_included == 30
+
+
+def test_inverse_square_sps_takes_nothing():
+    # tau <= B, so Theta_n / Theta_{n-1} <= B / (B + 1) < 1 for SPS = B^-2
+    c = synth.confidences(53, 6, 5, mean=4.0)
+    sps = 1.0 / np.arange(1, 65, dtype=np.float64) ** 2
+    res = oracle.schedule(c, sps)
+    assert (res.lengths == 0).all() and res.n_included == 0
+    assert res.theta_best == 6 * sps[5]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_greedy_equals_brute_force_when_unimodal(seed):
+    R, gamma = 3, 3
+    c = synth.confidences(60 + seed, R, gamma, mean=1.0, sd=1.5)
+    B = np.arange(1, 13, dtype=np.float64)
+    sps = 100.0 / (1.0 + 0.15 * B + 0.01 * B * B)
+    a = oracle.survival_products(c)
+    best = max(_theta(a, ell, sps) for ell in itertools.product(range(gamma + 1), repeat=R))
+    res = oracle.schedule(c, sps)
+    assert abs(res.theta_best - best) <= 1e-9 * best
+    assert abs(_theta(a, res.lengths, sps) - best) <= 1e-9 * best
+
+
+def test_non_unimodal_stops_at_first_local_maximum():
+    """Theta dips and then rises past its first peak: the early-stop rule keeps the
+    first peak (the DSpark guide's break on Theta <= Theta_best), not the global one."""
+    R, gamma = 2, 3
+    c = np.full((R, gamma), 0.9, dtype=np.float32)
+    sps = np.array([10.0, 10.0, 10.0, 7.0, 9.0, 9.0, 9.0, 9.0])  # SPS(B) for B = 1..8
+    res = oracle.schedule(c, sps)
+    a = oracle.survival_products(c)
+    # B = 2 -> 3 rises (tau 2 -> 2.9, SPS 10); B = 4 drops (SPS 7): stop with one entry
+    assert res.n_included == 1 and list(res.lengths) == [1, 0]
+    glob = max(_theta(a, ell, sps) for ell in itertools.product(range(gamma + 1), repeat=R))
+    assert res.theta_best < glob
+
+
+def test_ties_go_to_lower_request_then_lower_position():
+    c = np.array([[1.0, 0.5], [1.0, 1.0]], dtype=np.float32)
+    # a = [[1, .5], [1, 1]]: pool order (1,r0,j0) (1,r1,j0) (1,r1,j1) (.5,r0,j1)
+    sps = np.full(8, 1.0)
+    res = oracle.schedule(c, sps, B_max=3)
+    assert list(res.lengths) == [1, 0]
+    res = oracle.schedule(c, sps, B_max=5)
+    assert list(res.lengths) == [1, 2]
+
+
+def test_batch_cap():
+    c = synth.confidences(54, 4, 7)
+    res = oracle.schedule(c, np.full(64, 1.0), B_max=6)
+    assert res.lengths.sum() == 2 and res.n_included == 2
+    with pytest.raises(ValueError):
+        oracle.schedule(c, np.full(64, 1.0), B_max=3)
+
+
+def test_equal_theta_stops():
+    # an entry with a = 0 adds to B but not to tau; with constant SPS, Theta stays equal -> stop
+    c = np.array([[1.0, 0.0, 1.0]], dtype=np.float32)
+    res = oracle.schedule(c, np.full(8, 2.0))
+    assert list(res.lengths) == [1]
+
+
+def test_fixed_point_reading_matches_real_arithmetic_on_random_cases():
+    """Reading R6 quantises a to 2^-48; away from exact ties it chooses what a
+    float64 evaluation of the same greedy loop chooses."""
+    for seed in range(5):
+        c = synth.confidences(70 + seed, 40, 7)
+        sps = synth.sps_table(512)
+        res = oracle.schedule(c, sps)
+        a = oracle.survival_products(c)
+        order = sorted(((a[r, j], r, j) for r in range(40) for j in range(7)), key=lambda e: (-e[0], e[1], e[2]))
+        tau, B, best, n = 40.0, 40, 40.0 * sps[39], 0
+        for av, r, j in order:
+            th = (tau + av) * sps[B]
+            if th <= best:
+                break
+            tau, B, best, n = tau + av, B + 1, th, n + 1
+        assert n == res.n_included
+        assert abs(best - res.theta_best) <= 1e-12 * best
