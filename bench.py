@@ -1,0 +1,334 @@
+#!/usr/bin/env python3
+"""Benchmark of the verification hot path on GB300.
+
+Workload (one "step"): chain speculative sampling with c* for R=64 requests,
+gamma=7 draft positions, V=151936 bf16 logits, temperature 1 -- one
+specv_verify_chain call over a batch resident in HBM (target [64, 8, V] +
+draft [64, 7, V] = 291.7 MB of logits).  Metric: verified draft positions per
+second (sum of l_r over the batch / step time), plus achieved HBM GB/s as a
+fraction of the measured copy bandwidth.
+
+`--impl reference` times the CPU oracle (the reference arm of this repo) on the
+same workload, one bounded sample of requests per step.
+
+Multi-GPU (torchrun): every rank verifies its own batch (requests are
+independent; no collective on the data path); value = all ranks' positions /
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+R, GAMMA, V, TEMP = 64, 7, 151936, 1.0
+METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of peak) at R=64,γ=7,V=151936"
+UNIT = "positions/s"
+WORKLOAD = "batched chain verify: R=64, gamma=7, V=151936 bf16, T=1.0, c* output"
+ALGO_BYTES = R * (GAMMA + 1) * V * 2 + R * GAMMA * V * 2      # every logit read once
+PROFILE = os.path.join(ROOT, "profiles", "chain_stats_batched_r64_g7_v151936.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "lossless_draft_verification_gb300", "csrc", f) for f in ("chain.cu", "common.cuh")]
+
+
+def _peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _profile_traffic():
+    """Per-launch DRAM traffic from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_h or not m_t or m_h.group(1) != _kernel_hash():
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_threads() -> int:
+    return 1
+
+
+def oracle_positions_per_s(case, budget_s: float):
+    """Run the oracle request by request until `budget_s` elapses; positions/s."""
+    import oracle
+    t64, d64 = case.target.f64, case.draft.f64
+    done, pos = 0, 0
+    t0 = time.perf_counter()
+    while done < case.R and time.perf_counter() - t0 < budget_s:
+        sl = slice(done, done + 1)
+        oracle.verify_chain(t64[sl], d64[sl], case.tokens[sl], case.uniforms[sl], case.temperature)
+        pos += case.gamma
+        done += 1
+    el = time.perf_counter() - t0
+    return pos / el, done, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    case = synth.chain_batched(seed=3, R=R)
+    t64, d64 = case.target.f64, case.draft.f64
+    # size one step so that the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle.verify_chain(t64[:1], d64[:1], case.tokens[:1], case.uniforms[:1], TEMP)
+    per_req = time.perf_counter() - t0
+    n_req = int(max(1, min(R, 120.0 / max(1e-3, per_req * (args.steps + args.warmup)))))
+    def step(i):
+        s = (i * n_req) % R
+        idx = [(s + j) % R for j in range(n_req)]
+        oracle.verify_chain(t64[idx], d64[idx], case.tokens[idx], case.uniforms[idx], TEMP)
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = args.steps * n_req * GAMMA / el
+    sample = f"{n_req} of {R} requests per step (gamma=7, V=151936), float64 numpy oracle"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cpu_threads(), "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import lossless_draft_verification_gb300 as specv
+    from lossless_draft_verification_gb300 import build as _build
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    specv.load()
+
+    case = synth.chain_batched(seed=3 + 1000 * rank, R=R)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    target = to_dev(case.target.raw.view(np.int16)).view(torch.bfloat16)
+    draft = to_dev(case.draft.raw.view(np.int16)).view(torch.bfloat16)
+    tokens = to_dev(case.tokens.astype(np.int32))
+    uniforms = to_dev(case.uniforms.astype(np.float32))
+    acc = torch.empty(R, dtype=torch.int32, device=dev)
+    tok = torch.empty(R, dtype=torch.int32, device=dev)
+    cst = torch.empty(R, GAMMA, dtype=torch.float32, device=dev)
+    nbytes = specv.specv_verify_chain_workspace_size(R, GAMMA, V, specv.SPECV_BF16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ptrs = (target.data_ptr(), draft.data_ptr(), specv.SPECV_BF16, tokens.data_ptr(), None, uniforms.data_ptr(),
+            R, GAMMA, V, TEMP, acc.data_ptr(), tok.data_ptr(), cst.data_ptr(), ws.data_ptr(), nbytes, sp)
+
+    def call():
+        st = specv.specv_verify_chain(*ptrs)
+        if st != 0:
+            raise specv.SpecvError(st, "specv_verify_chain")
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flushed before every timed step
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.fmean(times)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    positions = R * GAMMA                   # lengths = gamma for every request
+    value = world * positions / (ms_max * 1e-3)
+
+    # end-to-end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_t = torch.from_numpy(case.target.raw.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_d = torch.from_numpy(case.draft.raw.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_x = torch.from_numpy(case.tokens.astype(np.int32)).pin_memory()
+        h_u = torch.from_numpy(case.uniforms.astype(np.float32)).pin_memory()
+        n_e2e = max(3, min(args.steps, 30))
+        for _ in range(3):
+            specv.verify_chain(h_t, h_d, h_x, h_u, TEMP, workspace=ws)
+        torch.cuda.synchronize()
+        e_times = []
+        for _ in range(n_e2e):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            A_h, y_h, c_h = specv.verify_chain(h_t, h_d, h_x, h_u, TEMP, workspace=ws)
+            e.record(stream)
+            torch.cuda.synchronize()
+            e_times.append(s.elapsed_time(e))
+        e_ms = statistics.fmean(e_times)
+        e_t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        if dist is not None:
+            dist.all_reduce(e_t, op=dist.ReduceOp.MAX)
+        h2d = sum(t.numel() * t.element_size() for t in (h_t, h_d, h_x, h_u))
+        d2h = sum(t.numel() * t.element_size() for t in (A_h, y_h, c_h))
+        e2e = {"value": world * positions / (float(e_t.item()) * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": float(e_t.item())}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n_req, el = oracle_positions_per_s(case, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": _cpu_threads(), "kind": "oracle",
+               "sample": f"{n_req} of {R} requests ({n_req * GAMMA} positions) in {el:.1f} s, float64 numpy oracle, one thread"}
+
+    peak, peak_kind = _peak_hbm()
+    achieved = ALGO_BYTES / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": _profile_traffic(), "peak_source": peak_kind,
+            "kernel": "chain_stats + chain_finish (whole specv_verify_chain call)",
+            "algorithmic_bytes_per_launch": ALGO_BYTES}
+    if dist is not None:
+        dist.barrier()
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": WORKLOAD, "R": R, "gamma": GAMMA, "V": V, "temperature": TEMP,
+                          "batch_per_gpu": R, "parallelism": f"independent requests x{world}",
+                          "l2": "flushed (2x L2 write) before every timed step", "wall_s": wall},
+               "hbm_gbs": achieved, "hbm_frac": achieved / peak, "roofline": roof, "cpu_baseline": cpu,
+               "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--requests", type=int, default=R, help="R (smaller for profiling captures)")
+    args = ap.parse_args()
+    global R, ALGO_BYTES, WORKLOAD
+    if args.requests != R:
+        R = args.requests
+        ALGO_BYTES = R * (GAMMA + 1) * V * 2 + R * GAMMA * V * 2
+        WORKLOAD = WORKLOAD.replace("R=64", f"R={R}")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,242 @@
+/*
+ * specv.h -- C ABI of the GB300 lossless draft-verification library.
+ *
+ * The library implements, as CUDA kernels for sm_103a, the data-parallel step
+ * of lossless speculative decoding that sits between the target model's
+ * forward pass and the commit of tokens:
+ *
+ *   specv_verify_chain        chain speculative sampling (accept / first
+ *                             rejection / residual or bonus token) and, at
+ *                             temperature 0, greedy argmax verification
+ *   specv_verify_tree_greedy  greedy verification of a linearised candidate tree
+ *   specv_markov_draft        the DSpark Markov draft head, sampled position by position
+ *   specv_tv_accept           the analytic acceptance c* = 1 - 1/2 ||p_d - p_t||_1
+ *   specv_schedule            DSpark's greedy throughput scheduler
+ *
+ * Sources (cited per entry point below):
+ *   [DART notes]   "DART：把草稿并行生成之后，还要补上哪些依赖？", DART reading
+ *                  notes, zhongzhuzhou.org, 2026-10-14.
+ *   [DSpark guide] DSpark paper guide, personal-site-bgy.pages.dev/ai-notes/
+ *                  dspark-paper-guide.html.
+ *   [SD survey]    "投机解码综述", zhifeiding.github.io, 2026-11-02.
+ *
+ * Notation: q = target distribution, p = draft distribution (DART notes §2.3).
+ * q = softmax(target_logits / T), p = softmax(draft_logits / T); T = 0 selects
+ * greedy (argmax) verification.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array pointer is a caller-owned DEVICE pointer on the current CUDA
+ *    device, row-major and contiguous, aligned at least to its element size.
+ *    The library never allocates, frees or keeps pointers after a call returns.
+ *  - Scratch memory: each entry point takes a caller-owned device `workspace`
+ *    of at least specv_*_workspace_size(...) bytes, 256-byte aligned.  Its
+ *    first 256 bytes hold the device error word (see specv_read_device_error);
+ *    the rest needs no initialisation.  Two calls that may run concurrently
+ *    must not share a workspace.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL =
+ *    the legacy default stream).  No call synchronises; outputs are valid when
+ *    the stream reaches the point after the call.  Calls allocate nothing and
+ *    can be enqueued repeatedly with the same arguments.
+ *  - Host-side validation happens before anything is enqueued: a bad argument
+ *    returns SPECV_ERR_INVALID_ARG (or SPECV_ERR_UNSUPPORTED for a valid but
+ *    unsupported shape/device) and nothing is launched.  A launch failure
+ *    returns SPECV_ERR_CUDA.
+ *  - Bad data that only the device can see (a token id outside [0, V), a
+ *    uniform outside [0, 1), a malformed tree) never traps: the affected
+ *    request's outputs are set to -1 and the device error word records
+ *    SPECV_ERR_DEVICE_DATA; read it with specv_read_device_error.
+ *  - Logits may be float32 or bfloat16 (SPECV_F32 / SPECV_BF16).  All
+ *    arithmetic is float32; argmax compares the stored values exactly and
+ *    resolves ties to the lowest token id.  Logits must be finite.
+ *  - Thread-safe: no global state other than a per-device capability cache.
+ */
+#ifndef SPECV_H_
+#define SPECV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPECV_API __attribute__((visibility("default")))
+#else
+#define SPECV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECV_ABI_VERSION 1
+#define SPECV_MAX_GAMMA 32          /* draft positions per request (chain)        */
+#define SPECV_MAX_TREE_NODES 1024   /* nodes per tree including the root          */
+#define SPECV_MAX_TREE_DEPTH 64
+#define SPECV_MAX_SCHED_ENTRIES 8192 /* R * gamma for specv_schedule              */
+#define SPECV_MAX_MARKOV_RANK 1024
+
+typedef enum {
+  SPECV_OK = 0,
+  SPECV_ERR_INVALID_ARG = 1,   /* a host-visible argument is invalid; nothing enqueued */
+  SPECV_ERR_UNSUPPORTED = 2,   /* valid request the build cannot serve (device, size)   */
+  SPECV_ERR_CUDA = 3,          /* a CUDA call or launch failed                          */
+  SPECV_ERR_DEVICE_DATA = 4,   /* device-detected bad data (outputs of that request = -1) */
+  SPECV_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up                    */
+} specv_status;
+
+typedef enum { SPECV_F32 = 0, SPECV_BF16 = 1 } specv_dtype;
+
+/* ------------------------------------------------------------------ chain */
+
+/*
+ * specv_verify_chain -- chain speculative sampling over full-vocabulary logits.
+ *
+ * Follows [DART notes] §2.3 eq. (3)-(4), [DSpark guide] (verification rule,
+ * prefix survival, bonus token) and [SD survey] §1.2-§1.3.  For each request r
+ * with draft length l_r (lengths[r], or gamma when lengths == NULL):
+ *   for k = 0 .. l_r-1, left to right: accept x_k iff
+ *       uniforms[r,k,0] < min(1, q_k(x_k) / p_k(x_k))       (p_k(x_k) = 0 accepts)
+ *   the first rejection at k stops the chain: accepted_len[r] = k and
+ *       out_token[r] is drawn from the residual r(v) = [q_k(v) - p_k(v)]_+ / R
+ *       with the uniform uniforms[r,k,1] (R = sum_v [q_k - p_k]_+; if R == 0
+ *       the draw is from q_k);
+ *   with no rejection accepted_len[r] = l_r and out_token[r] is the bonus token
+ *       drawn from q_{l_r} with uniforms[r,l_r,1].
+ *   A draw from weights w uses the inverse CDF over ascending token id:
+ *       y = min{ v : sum_{v' <= v} w(v') > u * sum_v w(v) }.
+ * The committed tokens of request r are x_0 .. x_{A-1} followed by out_token[r]
+ * (A + 1 tokens).
+ *
+ * T == 0: greedy verification ([SD survey] §1.3): g_k = argmax target[r,k,:];
+ *   accepted_len = first k < l_r with x_k != g_k (else l_r); out_token = g_A.
+ *   `uniforms` is not read and may be NULL.
+ *
+ * c_star (optional, may be NULL): c*_{r,k} = 1 - 1/2 ||p_k - q_k||_1 for
+ *   k < l_r ([DSpark guide], analytic acceptance); NaN for k >= l_r.  At T = 0
+ *   it is 1 when argmax draft_k == argmax target_k, else 0.
+ *
+ * Arguments
+ *   target_logits  [R, gamma+1, V]  dtype   row (r,k) = target logits that verify x_k;
+ *                                            row (r,l_r) is the bonus row
+ *   draft_logits   [R, gamma, V]    dtype   may be NULL only if T == 0 and c_star == NULL
+ *   draft_tokens   [R, gamma]       int32   x_{r,k} in [0, V)
+ *   lengths        [R] int32 or NULL        0 <= l_r <= gamma
+ *   uniforms       [R, gamma+1, 2]  float32 in [0, 1); [.,.,0] accept test,
+ *                                            [.,.,1] residual/bonus draw
+ *   R >= 0, 0 <= gamma <= SPECV_MAX_GAMMA, V >= 1, temperature >= 0 (finite)
+ *   accepted_len   [R] int32 out    A_r, or -1 on device-detected bad data
+ *   out_token      [R] int32 out    correction or bonus token, or -1
+ *   c_star         [R, gamma] float32 out, or NULL
+ * Errors: SPECV_ERR_INVALID_ARG for NULL/negative/misaligned arguments or a
+ *   workspace that is too small; SPECV_ERR_UNSUPPORTED if V is beyond what the
+ *   kernels tile (specv_verify_chain_workspace_size returns 0 then).
+ */
+SPECV_API size_t specv_verify_chain_workspace_size(int R, int gamma, int V, specv_dtype dtype);
+SPECV_API specv_status specv_verify_chain(const void* target_logits, const void* draft_logits, specv_dtype dtype,
+                                const int32_t* draft_tokens, const int32_t* lengths, const float* uniforms,
+                                int R, int gamma, int V, float temperature,
+                                int32_t* accepted_len, int32_t* out_token, float* c_star,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ c* */
+
+/*
+ * specv_tv_accept -- analytic acceptance c*_{r,k} = 1 - 1/2 ||p_k - q_k||_1
+ * ([DSpark guide], the confidence head's supervision target; equal to
+ * sum_v min(p_k, q_k) = 1 - R by [DART notes] eq. (3)).
+ *   target_logits  [R, target_positions, V] dtype, rows k < gamma are used
+ *   draft_logits   [R, gamma, V] dtype
+ *   target_positions >= gamma (e.g. gamma + 1 when the bonus row is present)
+ *   c_star         [R, gamma] float32 out.  At T = 0: argmax agreement (1 or 0).
+ */
+SPECV_API size_t specv_tv_accept_workspace_size(int R, int gamma, int V, specv_dtype dtype);
+SPECV_API specv_status specv_tv_accept(const void* target_logits, const void* draft_logits, specv_dtype dtype,
+                             int R, int gamma, int target_positions, int V, float temperature,
+                             float* c_star, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ tree */
+
+/*
+ * specv_verify_tree_greedy -- greedy (T = 0) verification of a linearised
+ * candidate tree ([DART notes] §2.3 last paragraph and Algorithm 3 steps 9-10;
+ * [SD survey] §2.3).
+ *   Node 0 is the root (the committed prefix); node i >= 1 carries token
+ *   tokens[r,i] and has parent parents[r,i] with 0 <= parents[r,i] < i
+ *   (ancestors precede descendants).  Row i of target_logits is the target's
+ *   distribution after node i.  g_i = argmax row i (lowest id on ties).
+ *   Node i is accepted iff its parent is accepted and tokens[r,i] == g_{parent}.
+ *   i* = accepted node of greatest depth (lowest index on ties).
+ *   path_len[r] = depth of i*, path_nodes[r,:] = the nodes root->i* without the
+ *   root (-1 padded), out_token[r] = g_{i*} (correction / bonus token).
+ *   target_logits [R, N+1, V] dtype; parents, tokens [R, N+1] int32
+ *   (parents[r,0] = -1, tokens[r,0] ignored); 1 <= max_depth <= SPECV_MAX_TREE_DEPTH;
+ *   0 <= N, N+1 <= SPECV_MAX_TREE_NODES.
+ *   path_len [R], path_nodes [R, max_depth], out_token [R] int32 out.
+ *   A malformed tree (bad parent, depth > max_depth, token outside [0, V))
+ *   gives -1 outputs for that request and SPECV_ERR_DEVICE_DATA.
+ */
+SPECV_API size_t specv_verify_tree_greedy_workspace_size(int R, int N, int V, specv_dtype dtype);
+SPECV_API specv_status specv_verify_tree_greedy(const void* target_logits, specv_dtype dtype,
+                                      const int32_t* parents, const int32_t* tokens,
+                                      int R, int N, int V, int max_depth,
+                                      int32_t* path_len, int32_t* path_nodes, int32_t* out_token,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ Markov head */
+
+/*
+ * specv_markov_draft -- semi-autoregressive drafting with the DSpark Markov head
+ * ([DSpark guide]: p_k(v | x_0, x_<k) = softmax(U_k(v) + B(x_{k-1}, v)),
+ * B = W1 W2, W1 [V, rank] used as a row lookup, W2 [rank, V] as the projection).
+ *   x_0 = anchor[r].  For k = 1 .. gamma (sequentially):
+ *     L_k = U[r,k-1,:] + W1[x_{k-1},:] . W2            (float32 accumulation)
+ *     x_k = inverse-CDF draw from softmax(L_k / T) with uniforms[r,k-1]
+ *           (T = 0: argmax, lowest id on ties)
+ *   U [R, gamma, V] bf16, W1 [V, rank] bf16, W2 [rank, V] bf16,
+ *   anchor [R] int32, uniforms [R, gamma] float32 (may be NULL at T = 0).
+ *   draft_tokens [R, gamma] int32 out (x_1 .. x_gamma).
+ *   draft_logits [R, gamma, V] out or NULL: the raw L_k (before temperature)
+ *   in logits_out_dtype (SPECV_F32 or SPECV_BF16).
+ *   1 <= rank <= SPECV_MAX_MARKOV_RANK, rank % 16 == 0.
+ */
+SPECV_API size_t specv_markov_draft_workspace_size(int R, int gamma, int V, int rank);
+SPECV_API specv_status specv_markov_draft(const void* U, const void* W1, const void* W2,
+                                const int32_t* anchor, const float* uniforms,
+                                int R, int gamma, int V, int rank, float temperature,
+                                int32_t* draft_tokens, void* draft_logits, specv_dtype logits_out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ scheduler */
+
+/*
+ * specv_schedule -- DSpark's greedy throughput scheduler ([DSpark guide],
+ * scheduler section).  a_{r,j} = prod_{i<=j} c_{r,i} (float64, left to right);
+ * B = sum_r (1 + l_r); tau = sum_r (1 + sum_{j<=l_r} a_{r,j}); Theta = tau * SPS(B).
+ * All (r, j) form one pool sorted by a descending (ties: lower r, then lower j);
+ * entries are taken from the top while Theta rises; the first entry with
+ * Theta <= Theta_best (or B > B_max) stops the loop (early stop).
+ * tau is accumulated in fixed point with quantum 2^-48 (a truncated), so the
+ * result is exact and independent of summation order.
+ *   conf  [R, gamma] float32 in [0, 1]; sps [B_max] float64, sps[B-1] = SPS(B) > 0;
+ *   R <= B_max; R * gamma <= SPECV_MAX_SCHED_ENTRIES.
+ *   lengths [R] int32 out; theta_best [1] float64 out or NULL (tau in tokens x SPS).
+ *   A confidence outside [0, 1] (or NaN) gives lengths = -1 and SPECV_ERR_DEVICE_DATA.
+ */
+SPECV_API size_t specv_schedule_workspace_size(int R, int gamma);
+SPECV_API specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
+                            int32_t* lengths, double* theta_best,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ utilities */
+
+/* Waits for `stream`, copies the device error word of `workspace` into
+ * *status_out (SPECV_OK or SPECV_ERR_DEVICE_DATA / SPECV_ERR_TIMEOUT) and
+ * leaves it unchanged.  Each entry point clears the word when it starts. */
+SPECV_API specv_status specv_read_device_error(const void* workspace, void* stream, int32_t* status_out);
+
+SPECV_API const char* specv_status_string(specv_status status);
+SPECV_API int specv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECV_H_ */

@@ -1,0 +1,345 @@
+"""Python binding of the specv C ABI (lossless draft verification on GB300).
+
+Two layers, both argument marshalling only (every step of the computation runs
+in the CUDA library ``_lib/libspecv.so``):
+
+* ``specv_*`` -- one function per C entry point with the same name and
+  argument order; pointers are passed as integers (``tensor.data_ptr()``) and
+  the return value is the integer ``specv_status``.
+* ``verify_chain``, ``tv_accept``, ``verify_tree_greedy``, ``markov_draft``,
+  ``schedule`` -- tensor-level helpers: they check dtype/shape/device,
+  allocate outputs and the workspace with torch on the tensors' device, call
+  the C entry point on the current torch stream and raise ``SpecvError`` on a
+  non-zero status.  ``verify_chain`` also accepts host tensors: inputs are
+  copied to the device and the results back (the end-to-end path).
+
+There is no fallback: if the shared library is missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "load", "SpecvError", "SPECV_OK", "SPECV_ERR_INVALID_ARG", "SPECV_ERR_UNSUPPORTED", "SPECV_ERR_CUDA",
+    "SPECV_ERR_DEVICE_DATA", "SPECV_ERR_TIMEOUT", "SPECV_F32", "SPECV_BF16", "EXPORTED",
+    "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_tv_accept_workspace_size", "specv_tv_accept",
+    "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
+    "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_read_device_error",
+    "specv_status_string", "specv_abi_version",
+    "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "read_device_error",
+]
+
+SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_DEVICE_DATA, SPECV_ERR_TIMEOUT = range(6)
+SPECV_F32, SPECV_BF16 = 0, 1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libspecv.so")
+
+_c_int, _c_size, _c_float, _c_double, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
+
+# name -> (restype, argtypes); every symbol declared in include/specv.h
+EXPORTED = {
+    "specv_verify_chain_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "specv_verify_chain": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
+                                    _vp, _c_size, _vp]),
+    "specv_tv_accept_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "specv_tv_accept": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _c_size, _vp]),
+    "specv_verify_tree_greedy_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "specv_verify_tree_greedy": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp,
+                                          _c_size, _vp]),
+    "specv_markov_draft_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "specv_markov_draft": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp,
+                                    _c_int, _vp, _c_size, _vp]),
+    "specv_schedule_workspace_size": (_c_size, [_c_int, _c_int]),
+    "specv_schedule": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "specv_read_device_error": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
+    "specv_status_string": (ctypes.c_char_p, [_c_int]),
+    "specv_abi_version": (_c_int, []),
+}
+
+_lib = None
+
+
+class SpecvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libspecv.so (built by lossless_draft_verification_gb300.build)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FileNotFoundError(f"{p} is missing: build it with `python -m lossless_draft_verification_gb300.build`")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in EXPORTED.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().specv_status_string(status).decode()
+
+
+def _call(name, *args):
+    return getattr(load(), name)(*args)
+
+
+# --------------------------------------------------------------------------- raw entry points
+def specv_verify_chain_workspace_size(R, gamma, V, dtype):
+    return _call("specv_verify_chain_workspace_size", R, gamma, V, dtype)
+
+
+def specv_verify_chain(target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms, R, gamma, V, temperature,
+                       accepted_len, out_token, c_star, workspace, workspace_bytes, stream):
+    return _call("specv_verify_chain", target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms, R, gamma,
+                 V, temperature, accepted_len, out_token, c_star, workspace, workspace_bytes, stream)
+
+
+def specv_tv_accept_workspace_size(R, gamma, V, dtype):
+    return _call("specv_tv_accept_workspace_size", R, gamma, V, dtype)
+
+
+def specv_tv_accept(target_logits, draft_logits, dtype, R, gamma, target_positions, V, temperature, c_star, workspace,
+                    workspace_bytes, stream):
+    return _call("specv_tv_accept", target_logits, draft_logits, dtype, R, gamma, target_positions, V, temperature,
+                 c_star, workspace, workspace_bytes, stream)
+
+
+def specv_verify_tree_greedy_workspace_size(R, N, V, dtype):
+    return _call("specv_verify_tree_greedy_workspace_size", R, N, V, dtype)
+
+
+def specv_verify_tree_greedy(target_logits, dtype, parents, tokens, R, N, V, max_depth, path_len, path_nodes,
+                             out_token, workspace, workspace_bytes, stream):
+    return _call("specv_verify_tree_greedy", target_logits, dtype, parents, tokens, R, N, V, max_depth, path_len,
+                 path_nodes, out_token, workspace, workspace_bytes, stream)
+
+
+def specv_markov_draft_workspace_size(R, gamma, V, rank):
+    return _call("specv_markov_draft_workspace_size", R, gamma, V, rank)
+
+
+def specv_markov_draft(U, W1, W2, anchor, uniforms, R, gamma, V, rank, temperature, draft_tokens, draft_logits,
+                       logits_out_dtype, workspace, workspace_bytes, stream):
+    return _call("specv_markov_draft", U, W1, W2, anchor, uniforms, R, gamma, V, rank, temperature, draft_tokens,
+                 draft_logits, logits_out_dtype, workspace, workspace_bytes, stream)
+
+
+def specv_schedule_workspace_size(R, gamma):
+    return _call("specv_schedule_workspace_size", R, gamma)
+
+
+def specv_schedule(conf, sps, R, gamma, B_max, lengths, theta_best, workspace, workspace_bytes, stream):
+    return _call("specv_schedule", conf, sps, R, gamma, B_max, lengths, theta_best, workspace, workspace_bytes, stream)
+
+
+def specv_read_device_error(workspace, stream, status_out):
+    return _call("specv_read_device_error", workspace, stream, status_out)
+
+
+def specv_status_string(status):
+    return _call("specv_status_string", status)
+
+
+def specv_abi_version():
+    return _call("specv_abi_version")
+
+
+# --------------------------------------------------------------------------- tensor helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return SPECV_BF16
+    if t.dtype == torch.float32:
+        return SPECV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, device, dtype=None, shape=None):
+    if t is None:
+        return
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _raise(status, where):
+    if status != SPECV_OK:
+        raise SpecvError(status, where)
+
+
+def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, lengths=None, want_c_star: bool = True,
+                 workspace=None, stream=None, out=None):
+    """Chain speculative sampling (see specv_verify_chain in include/specv.h).
+
+    target [R, gamma+1, V], draft [R, gamma, V] (bf16 or float32), draft_tokens
+    [R, gamma] int32, uniforms [R, gamma+1, 2] float32 (None at T = 0), lengths
+    [R] int32 or None.  Returns (accepted_len [R], out_token [R], c_star [R, gamma]
+    or None) on the inputs' device.  Host (CPU) inputs are copied to the current
+    CUDA device first and the results copied back."""
+    torch = _torch()
+    host = target.device.type == "cpu"
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        nb = target.is_pinned()
+        target = target.to(dev, non_blocking=nb)
+        draft = None if draft is None else draft.to(dev, non_blocking=nb)
+        draft_tokens = draft_tokens.to(dev, non_blocking=nb)
+        uniforms = None if uniforms is None else uniforms.to(dev, non_blocking=nb)
+        lengths = None if lengths is None else lengths.to(dev, non_blocking=nb)
+    R, P, V = target.shape
+    gamma = P - 1
+    dev = target.device
+    _check(target, "target", dev)
+    _check(draft, "draft", dev, target.dtype, (R, gamma, V))
+    _check(draft_tokens, "draft_tokens", dev, torch.int32, (R, gamma))
+    _check(uniforms, "uniforms", dev, torch.float32, (R, gamma + 1, 2))
+    _check(lengths, "lengths", dev, torch.int32, (R,))
+    code = _dtype_code(target)
+    if out is None:
+        acc = torch.empty(R, dtype=torch.int32, device=dev)
+        tok = torch.empty(R, dtype=torch.int32, device=dev)
+        cst = torch.empty(R, gamma, dtype=torch.float32, device=dev) if want_c_star else None
+    else:
+        acc, tok, cst = out
+    nbytes = specv_verify_chain_workspace_size(R, gamma, V, code)
+    if nbytes == 0:
+        raise SpecvError(SPECV_ERR_UNSUPPORTED, "specv_verify_chain_workspace_size")
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_verify_chain(_p(target), _p(draft), code, _p(draft_tokens), _p(lengths), _p(uniforms), R, gamma, V,
+                            float(temperature), _p(acc), _p(tok), _p(cst), _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_verify_chain")
+    if host:
+        return acc.cpu(), tok.cpu(), None if cst is None else cst.cpu()
+    return acc, tok, cst
+
+
+def tv_accept(target, draft, temperature: float, workspace=None, stream=None):
+    """c*_{r,k} = 1 - 1/2 ||p_k - q_k||_1 for target [R, P >= gamma, V], draft [R, gamma, V]."""
+    torch = _torch()
+    R, P, V = target.shape
+    gamma = draft.shape[1]
+    dev = target.device
+    _check(target, "target", dev)
+    _check(draft, "draft", dev, target.dtype, (R, gamma, V))
+    code = _dtype_code(target)
+    cst = torch.empty(R, gamma, dtype=torch.float32, device=dev)
+    nbytes = specv_tv_accept_workspace_size(R, gamma, V, code)
+    if nbytes == 0:
+        raise SpecvError(SPECV_ERR_UNSUPPORTED, "specv_tv_accept_workspace_size")
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_tv_accept(_p(target), _p(draft), code, R, gamma, P, V, float(temperature), _p(cst), _p(ws), ws.numel(),
+                         _stream_ptr(stream))
+    _raise(st, "specv_tv_accept")
+    return cst
+
+
+def verify_tree_greedy(target, parents, tokens, max_depth: int, workspace=None, stream=None):
+    """Greedy tree verification; target [R, N+1, V], parents/tokens [R, N+1] int32.
+    Returns (path_len [R], path_nodes [R, max_depth], out_token [R])."""
+    torch = _torch()
+    R, N1, V = target.shape
+    dev = target.device
+    _check(target, "target", dev)
+    _check(parents, "parents", dev, torch.int32, (R, N1))
+    _check(tokens, "tokens", dev, torch.int32, (R, N1))
+    code = _dtype_code(target)
+    plen = torch.empty(R, dtype=torch.int32, device=dev)
+    nodes = torch.empty(R, max_depth, dtype=torch.int32, device=dev)
+    tok = torch.empty(R, dtype=torch.int32, device=dev)
+    nbytes = specv_verify_tree_greedy_workspace_size(R, N1 - 1, V, code)
+    if nbytes == 0:
+        raise SpecvError(SPECV_ERR_UNSUPPORTED, "specv_verify_tree_greedy_workspace_size")
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_verify_tree_greedy(_p(target), code, _p(parents), _p(tokens), R, N1 - 1, V, int(max_depth), _p(plen),
+                                  _p(nodes), _p(tok), _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_verify_tree_greedy")
+    return plen, nodes, tok
+
+
+def markov_draft(U, W1, W2, anchor, uniforms, temperature: float, want_logits: bool = True, logits_dtype=None,
+                 workspace=None, stream=None):
+    """Markov-head drafting; U [R, gamma, V], W1 [V, rank], W2 [rank, V] bf16, anchor [R]
+    int32, uniforms [R, gamma] float32.  Returns (draft_tokens [R, gamma], logits or None)."""
+    torch = _torch()
+    R, gamma, V = U.shape
+    rank = W1.shape[1]
+    dev = U.device
+    _check(U, "U", dev, torch.bfloat16)
+    _check(W1, "W1", dev, torch.bfloat16, (V, rank))
+    _check(W2, "W2", dev, torch.bfloat16, (rank, V))
+    _check(anchor, "anchor", dev, torch.int32, (R,))
+    _check(uniforms, "uniforms", dev, torch.float32, (R, gamma))
+    toks = torch.empty(R, gamma, dtype=torch.int32, device=dev)
+    ldt = logits_dtype or torch.float32
+    logits = torch.empty(R, gamma, V, dtype=ldt, device=dev) if want_logits else None
+    code = SPECV_BF16 if ldt == torch.bfloat16 else SPECV_F32
+    nbytes = specv_markov_draft_workspace_size(R, gamma, V, rank)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_markov_draft(_p(U), _p(W1), _p(W2), _p(anchor), _p(uniforms), R, gamma, V, rank, float(temperature),
+                            _p(toks), _p(logits), code, _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_markov_draft")
+    return toks, logits
+
+
+def schedule(conf, sps, B_max: int | None = None, workspace=None, stream=None):
+    """Greedy throughput scheduler; conf [R, gamma] float32, sps [B_max] float64.
+    Returns (lengths [R] int32, theta_best [1] float64)."""
+    torch = _torch()
+    R, gamma = conf.shape
+    dev = conf.device
+    _check(conf, "conf", dev, torch.float32)
+    _check(sps, "sps", dev, torch.float64)
+    B_max = sps.shape[0] if B_max is None else B_max
+    lengths = torch.empty(R, dtype=torch.int32, device=dev)
+    theta = torch.empty(1, dtype=torch.float64, device=dev)
+    nbytes = specv_schedule_workspace_size(R, gamma)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_schedule(_p(conf), _p(sps), R, gamma, int(B_max), _p(lengths), _p(theta), _p(ws), ws.numel(),
+                        _stream_ptr(stream))
+    _raise(st, "specv_schedule")
+    return lengths, theta
+
+
+def read_device_error(workspace, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    st = specv_read_device_error(_p(workspace), _stream_ptr(stream), ctypes.byref(out))
+    _raise(st, "specv_read_device_error")
+    return out.value

@@ -1,0 +1,208 @@
+// DSpark's greedy throughput scheduler (sm_103a), one CTA.
+//
+// Method (DSpark paper guide, scheduler section): a_{r,j} = prod_{i<=j} c_{r,i};
+// every (r, j) enters one pool sorted by a descending; entries are taken from
+// the top, each adding 1 to the verify batch B and a_{r,j} to the expected
+// accepted count tau; Theta = tau * SPS(B); the loop stops at the first entry
+// with Theta <= Theta_best.  Because a_{r,j} does not increase with j, the
+// taken entries of each request form a prefix and l_r is their count.
+//
+// Parallel form: survival products (float64, left to right, one thread per
+// request), a bitonic sort of (a, index) pairs in shared memory, a block-wide
+// int64 prefix sum of the fixed-point increments floor(a * 2^48) (exact, so
+// identical to any sequential order), Theta_n for every n at once, and a
+// block minimum over the first descent.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace specv {
+
+constexpr int kSchedThreads = 1024;
+constexpr double kQuantum = 281474976710656.0;   // 2^48
+
+struct SchedArgs {
+  const float* conf;
+  const double* sps;
+  void* workspace;
+  int32_t* lengths;
+  double* theta_best;
+  int R, gamma, B_max, n_pad;
+};
+
+__device__ __forceinline__ bool pair_less(unsigned long long ka, int ia, unsigned long long kb, int ib) {
+  return ka < kb || (ka == kb && ia < ib);
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int n_pad = a.n_pad;
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);     // ~bits(a): ascending = a descending
+  int* idx = reinterpret_cast<int*>(key + n_pad);
+  long long* pre = reinterpret_cast<long long*>(idx + n_pad);                // inclusive prefix of aQ (sorted)
+  int* ell = reinterpret_cast<int*>(pre + n_pad);                           // [R]
+  __shared__ long long s_warp[kSchedThreads / 32];
+  __shared__ int s_first;
+  __shared__ int s_bad;
+
+  const int tid = threadIdx.x;
+  const int R = a.R, gamma = a.gamma, n = R * gamma;
+  if (tid == 0) {
+    *reinterpret_cast<int*>(a.workspace) = 0;
+    s_first = n + 1;
+    s_bad = 0;
+  }
+  for (int i = tid; i < R; i += kSchedThreads) ell[i] = 0;
+
+  // survival products, one request per thread
+  for (int r = tid; r < R; r += kSchedThreads) {
+    double prod = 1.0;
+    for (int j = 0; j < gamma; ++j) {
+      const float c = a.conf[size_t(r) * gamma + j];
+      if (!(c >= 0.f && c <= 1.f)) s_bad = 1;
+      prod = __dmul_rn(prod, double(c));
+      key[r * gamma + j] = ~static_cast<unsigned long long>(__double_as_longlong(prod));
+      idx[r * gamma + j] = r * gamma + j;
+    }
+  }
+  for (int i = n + tid; i < n_pad; i += kSchedThreads) {
+    key[i] = ~0ull;
+    idx[i] = 0x7fffffff;
+  }
+  __syncthreads();
+
+  // bitonic sort of (key, idx), ascending
+  for (int size = 2; size <= n_pad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n_pad / 2; i += kSchedThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long k0 = key[lo], k1 = key[hi];
+        const int i0 = idx[lo], i1 = idx[hi];
+        const bool swap = up ? pair_less(k1, i1, k0, i0) : pair_less(k0, i0, k1, i1);
+        if (swap) {
+          key[lo] = k1; key[hi] = k0;
+          idx[lo] = i1; idx[hi] = i0;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // fixed-point increments and their inclusive prefix (contiguous chunk per thread)
+  const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
+  const int b0 = tid * per;
+  long long run = 0;
+  for (int i = b0; i < b0 + per && i < n_pad; ++i) {
+    long long q = 0;
+    if (i < n) q = __double2ll_rz(__dmul_rn(__longlong_as_double(static_cast<long long>(~key[i])), kQuantum));
+    run += q;
+    pre[i] = run;
+  }
+  // block exclusive scan of the per-thread totals
+  const int lane = tid & 31, warp = tid >> 5;
+  long long v = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const long long offset = (warp > 0 ? s_warp[warp - 1] : 0) + (v - run);
+  for (int i = b0; i < b0 + per && i < n_pad; ++i) pre[i] += offset;
+  __syncthreads();
+
+  // Theta_m for m entries taken (m = 0 .. n); first m >= 1 that does not rise
+  const long long tau0 = static_cast<long long>(R) * static_cast<long long>(kQuantum);
+  auto theta = [&](int m) -> double {          // m entries taken, requires R + m <= B_max
+    const long long tau = tau0 + (m > 0 ? pre[m - 1] : 0);
+    return __dmul_rn(__ll2double_rn(tau), a.sps[R + m - 1]);
+  };
+  for (int m = 1 + tid; m <= n; m += kSchedThreads) {
+    bool stop = R + m > a.B_max;
+    if (!stop) {
+      const double t = theta(m), tp = theta(m - 1);
+      stop = !(t > tp);
+      if (!(a.sps[R + m - 1] > 0.0)) s_bad = 1;
+    }
+    if (stop) atomicMin(&s_first, m);
+  }
+  if (!(a.sps[R - 1] > 0.0) && tid == 0) s_bad = 1;
+  __syncthreads();
+  const int taken = s_first - 1;
+  for (int i = tid; i < taken; i += kSchedThreads) atomicAdd(&ell[idx[i] / gamma], 1);
+  __syncthreads();
+  const bool bad = s_bad != 0;
+  for (int r = tid; r < R; r += kSchedThreads) a.lengths[r] = bad ? -1 : ell[r];
+  if (tid == 0) {
+    if (a.theta_best) a.theta_best[0] = bad ? __longlong_as_double(0x7ff8000000000000ll) : theta(taken) / kQuantum;
+    if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
+  }
+}
+
+namespace {
+int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+size_t sched_smem(int R, int n_pad) {
+  return size_t(n_pad) * (sizeof(unsigned long long) + sizeof(int) + sizeof(long long)) + size_t(R) * sizeof(int);
+}
+}  // namespace
+
+}  // namespace specv
+
+using namespace specv;
+
+extern "C" size_t specv_schedule_workspace_size(int R, int gamma) {
+  if (R < 0 || gamma < 0 || size_t(R) * gamma > SPECV_MAX_SCHED_ENTRIES) return 0;
+  return kHeaderBytes;
+}
+
+extern "C" specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
+                                       int32_t* lengths, double* theta_best, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (R < 0 || gamma < 0 || B_max < 1 || size_t(R) * gamma > SPECV_MAX_SCHED_ENTRIES || R > B_max)
+    return SPECV_ERR_INVALID_ARG;
+  if (R == 0) return SPECV_OK;
+  if ((gamma > 0 && !conf) || !sps || !lengths || !workspace) return SPECV_ERR_INVALID_ARG;
+  if (!aligned_to(conf, 4) || !aligned_to(sps, 8) || !aligned_to(lengths, 4) || !aligned_to(theta_best, 8) ||
+      !aligned_to(workspace, 256))
+    return SPECV_ERR_INVALID_ARG;
+  if (workspace_bytes < kHeaderBytes) return SPECV_ERR_INVALID_ARG;
+  specv_status s = check_device();
+  if (s != SPECV_OK) return s;
+  SchedArgs sa;
+  sa.conf = conf;
+  sa.sps = sps;
+  sa.workspace = workspace;
+  sa.lengths = lengths;
+  sa.theta_best = theta_best;
+  sa.R = R;
+  sa.gamma = gamma;
+  sa.B_max = B_max;
+  sa.n_pad = pow2_at_least(R * gamma < 2 ? 2 : R * gamma);
+  const size_t smem = sched_smem(R, sa.n_pad);
+  const void* fn = reinterpret_cast<const void*>(&schedule_kernel);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  void* args[] = {&sa};
+  if (cudaLaunchKernel(fn, dim3(1), dim3(kSchedThreads), args, smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  return SPECV_OK;
+}

@@ -18,5 +18,7 @@ def lib():
     """The CUDA library through its Python binding; the binding raises if the
     shared object is missing, so GPU tests never run on a fallback."""
     import lossless_draft_verification_gb300 as specv
+    from lossless_draft_verification_gb300 import build
+    build.build()
     specv.load()
     return specv

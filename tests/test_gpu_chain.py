@@ -1,0 +1,173 @@
+"""CUDA vs oracle parity for specv_verify_chain and specv_tv_accept.
+
+Sizes span several warp tiles, a cluster of CTAs and ragged tails; the last
+tests run the batched workload at full size (R=64, gamma=7, V=151936 bf16) in
+the launch configuration the benchmark times."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import TOL, check_chain, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_chain(lib, case, want_c_star=True):
+    import torch
+    dev = torch.device("cuda")
+    target = to_torch(case.target, dev)
+    draft = to_torch(case.draft, dev)
+    tok = to_torch(case.tokens, dev, np.int32)
+    u = to_torch(case.uniforms, dev, np.float32)
+    lengths = None if case.lengths is None else to_torch(case.lengths, dev, np.int32)
+    A, y, c = lib.verify_chain(target, draft, tok, u, case.temperature, lengths, want_c_star)
+    torch.cuda.synchronize()
+    return A.cpu().numpy(), y.cpu().numpy(), None if c is None else c.cpu().numpy()
+
+
+def _check_sampling(lib, case):
+    A, y, c = _run_chain(lib, case)
+    t64, d64 = case.target.f64, case.draft.f64
+    T = case.temperature
+    res = oracle.verify_chain(t64, d64, case.tokens, case.uniforms, T, case.lengths)
+    ell = case.lengths if case.lengths is not None else np.full(case.R, case.gamma)
+    st = check_chain(A, y, res, lambda r, k: oracle.softmax_t(t64[r, k], T),
+                     lambda r, k: oracle.softmax_t(d64[r, k], T), case.uniforms, ell)
+    ok = ~np.isnan(res.c_star)
+    assert (np.isnan(c) == ~ok).all(), "c* NaN pattern differs"
+    assert np.abs(c[ok] - res.c_star[ok]).max(initial=0.0) <= TOL
+    return st, A, y, res
+
+
+def _check_greedy(lib, case):
+    A, y, c = _run_chain(lib, case)
+    acc, tok, cst, _ = oracle.verify_chain_greedy(case.target.f64, case.tokens, case.lengths, case.draft.f64)
+    assert (A == acc).all() and (y == tok).all()
+    ok = ~np.isnan(cst)
+    assert (np.isnan(c) == ~ok).all() and (c[ok] == cst[ok]).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1024, 1000, 4099, 50000])
+def test_chain_sampling_small(lib, dtype, V):
+    case = synth.chain_batched(seed=101, R=12, gamma=5, V=V, dtype=dtype, ragged_lengths=True)
+    st, A, _, res = _check_sampling(lib, case)
+    assert st.exact >= st.n - 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1024, 1001, 70000])
+def test_chain_greedy_small(lib, dtype, V):
+    case = synth.chain_batched(seed=102, R=10, gamma=6, V=V, dtype=dtype, temperature=0.0, ragged_lengths=True)
+    # make some drafts agree with the target argmax so accepted prefixes vary
+    g = np.argmax(case.target.f64, -1)
+    coin = synth.uniform_u24(102, 40, case.tokens.shape) < 0.7
+    case.tokens = np.where(coin, g[:, :case.gamma], case.tokens).astype(np.int32)
+    _check_greedy(lib, case)
+
+
+def test_tiny_chain_config(lib):
+    """R=1, gamma=4, V=1024 float32 at T=1 and T=0."""
+    for T in (1.0, 0.0):
+        case = synth.chain_tiny(seed=1, temperature=T)
+        if T > 0:
+            _check_sampling(lib, case)
+        else:
+            _check_greedy(lib, case)
+
+
+@pytest.mark.parametrize("T", [0.5, 1.0, 2.5])
+def test_temperatures(lib, T):
+    case = synth.chain_batched(seed=103, R=8, gamma=4, V=3000, dtype="bf16", temperature=T)
+    _check_sampling(lib, case)
+
+
+def test_equal_distributions_accept_everything(lib):
+    case = synth.chain_batched(seed=104, R=6, gamma=5, V=2048, dtype="bf16")
+    case.draft.raw[:] = case.target.raw[:, :case.gamma]
+    A, y, c = _run_chain(lib, case)
+    assert (A == case.gamma).all()
+    np.testing.assert_allclose(c, 1.0, atol=TOL)
+    _check_sampling(lib, case)
+
+
+def test_disjoint_support_rejects_and_draws_from_q(lib):
+    V, R, gamma = 512, 16, 3
+    case = synth.chain_batched(seed=105, R=R, gamma=gamma, V=V, dtype="f32")
+    t = case.target.raw
+    d = case.draft.raw
+    t[:, :, V // 2:] = -np.inf            # q lives on the lower half
+    d[:, :, : V // 2] = -np.inf           # p lives on the upper half
+    case.tokens = synth.gumbel_max_tokens(case.draft.f64, 1.0, 105, 9)
+    A, y, c = _run_chain(lib, case)
+    assert (A == 0).all() and (y < V // 2).all()
+    np.testing.assert_allclose(c, 0.0, atol=TOL)
+    _check_sampling(lib, case)
+
+
+def test_bonus_only_and_degenerate_sizes(lib):
+    # gamma = 0: only the bonus draw
+    case = synth.chain_batched(seed=106, R=5, gamma=0, V=777, dtype="f32")
+    _check_sampling(lib, case)
+    # V = 1: every token is 0
+    case = synth.chain_batched(seed=107, R=3, gamma=2, V=1, dtype="f32")
+    case.tokens[:] = 0
+    A, y, c = _run_chain(lib, case)
+    assert (A == 2).all() and (y == 0).all()
+    np.testing.assert_allclose(c, 1.0, atol=TOL)
+
+
+def test_bad_token_sets_device_error(lib):
+    import torch
+    case = synth.chain_batched(seed=108, R=4, gamma=3, V=640, dtype="bf16")
+    case.tokens[2, 1] = 640               # out of range
+    dev = torch.device("cuda")
+    target, draft = to_torch(case.target, dev), to_torch(case.draft, dev)
+    tok, u = to_torch(case.tokens, dev, np.int32), to_torch(case.uniforms, dev, np.float32)
+    nbytes = lib.specv_verify_chain_workspace_size(4, 3, 640, lib.SPECV_BF16)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    A, y, _ = lib.verify_chain(target, draft, tok, u, 1.0, None, False, workspace=ws)
+    A, y = A.cpu().numpy(), y.cpu().numpy()
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+    ok = [0, 1, 3]
+    if A[2] != -1:
+        # the bad token sits after an earlier rejection only if A[2] < 1
+        assert A[2] == 0
+    assert (A[ok] >= 0).all()
+    # a clean call clears the word
+    case.tokens[2, 1] = 0
+    lib.verify_chain(target, draft, to_torch(case.tokens, dev, np.int32), u, 1.0, None, False, workspace=ws)
+    assert lib.read_device_error(ws) == lib.SPECV_OK
+
+
+def test_tv_accept_matches_oracle(lib):
+    import torch
+    dev = torch.device("cuda")
+    for dtype, V in (("bf16", 151936), ("f32", 3001)):
+        case = synth.chain_batched(seed=109, R=3, gamma=4, V=V, dtype=dtype)
+        target, draft = to_torch(case.target, dev), to_torch(case.draft, dev)
+        for T in (1.0, 0.7):
+            c = lib.tv_accept(target, draft, T).cpu().numpy()
+            ref = oracle.tv_accept(case.target.f64, case.draft.f64, T)
+            assert np.abs(c - ref).max() <= TOL
+        c0 = lib.tv_accept(target, draft, 0.0).cpu().numpy()
+        assert (c0 == oracle.tv_accept(case.target.f64, case.draft.f64, 0.0)).all()
+
+
+def test_long_vocab_single_request(lib):
+    """R=1, gamma=7, V=151936 bf16, one planted +8 peak per position, T=1 and T=0."""
+    case = synth.chain_long_vocab(seed=2)
+    _check_sampling(lib, case)
+    g = synth.chain_long_vocab(seed=2, temperature=0.0)
+    _check_greedy(lib, g)
+
+
+def test_batched_full_size(lib):
+    """The benchmarked workload: R=64, gamma=7, V=151936 bf16, T=1, every request
+    and every c*_{r,k} checked against the oracle."""
+    case = synth.chain_batched(seed=3)
+    st, A, y, res = _check_sampling(lib, case)
+    print(f"\nbatched full size: {st.n} requests, {st.exact} exact, flagged accept {st.flagged_accept}, "
+          f"flagged sample {st.flagged_sample}, mean accepted {A.mean():.2f} (oracle {res.accepted.mean():.2f})")
+    assert st.exact >= st.n - 8

@@ -1,0 +1,203 @@
+"""CUDA vs oracle parity for specv_verify_tree_greedy, specv_markov_draft and
+specv_schedule.  Tree paths and scheduler lengths are bit-exact; Markov logits
+agree within a float32-accumulation bound and sampled tokens follow the
+flagged-threshold rule, checked step by step with the GPU's own previous token
+as the conditioning input."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import TOL, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+# --------------------------------------------------------------------------- tree
+def _run_tree(lib, case):
+    import torch
+    dev = torch.device("cuda")
+    plen, nodes, tok = lib.verify_tree_greedy(to_torch(case.target, dev), to_torch(case.parents, dev, np.int32),
+                                              to_torch(case.tokens, dev, np.int32), case.max_depth)
+    return plen.cpu().numpy(), nodes.cpu().numpy(), tok.cpu().numpy()
+
+
+def _check_tree(lib, case):
+    plen, nodes, tok = _run_tree(lib, case)
+    ref = oracle.verify_tree_greedy(case.target.f64, case.parents, case.tokens, case.max_depth)
+    assert (plen == ref.path_len).all()
+    assert (nodes == ref.path_nodes).all()
+    assert (tok == ref.token).all()
+    return ref
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 4096), ("f32", 999), ("bf16", 33001)])
+def test_tree_small(lib, dtype, V):
+    case = synth.tree_greedy(seed=201, R=6, N=25, max_depth=6, V=V, dtype=dtype, p_follow=0.8)
+    ref = _check_tree(lib, case)
+    assert ref.path_len.max() >= 2
+
+
+def test_tree_degenerate(lib):
+    # a root-only tree and a single chain
+    case = synth.tree_greedy(seed=202, R=3, N=0, max_depth=1, V=100, dtype="f32")
+    _check_tree(lib, case)
+    case = synth.tree_greedy(seed=203, R=4, N=8, max_depth=8, V=300, dtype="f32", p_follow=0.9)
+    case.parents[:] = np.arange(-1, 8)
+    _check_tree(lib, case)
+
+
+def test_tree_bad_parent_sets_error(lib):
+    import torch
+    case = synth.tree_greedy(seed=204, R=3, N=10, max_depth=5, V=256, dtype="f32")
+    case.parents[1, 4] = 7                       # a child before its parent
+    dev = torch.device("cuda")
+    nbytes = lib.specv_verify_tree_greedy_workspace_size(3, 10, 256, lib.SPECV_F32)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    plen, nodes, tok = lib.verify_tree_greedy(to_torch(case.target, dev), to_torch(case.parents, dev, np.int32),
+                                              to_torch(case.tokens, dev, np.int32), 5, workspace=ws)
+    plen = plen.cpu().numpy()
+    assert plen[1] == -1 and plen[0] >= 0 and plen[2] >= 0
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+
+
+def test_tree_full_size(lib):
+    """R=16 trees of 60 nodes + root, depth <= 8, V=151936 bf16."""
+    case = synth.tree_greedy(seed=4)
+    ref = _check_tree(lib, case)
+    print(f"\ntree full size: mean accepted path {ref.path_len.mean():.2f}, max {ref.path_len.max()}")
+
+
+# --------------------------------------------------------------------------- Markov head
+def _markov_check(lib, m, T, logits_dtype="f32"):
+    import torch
+    dev = torch.device("cuda")
+    U, W1, W2 = to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev)
+    anchor = to_torch(m.anchor, dev, np.int32)
+    u = to_torch(m.uniforms, dev, np.float32)
+    ldt = torch.bfloat16 if logits_dtype == "bf16" else torch.float32
+    toks, logits = lib.markov_draft(U, W1, W2, anchor, u, T, True, ldt)
+    toks = toks.cpu().numpy()
+    L = logits.float().cpu().numpy().astype(np.float64)
+    U64, W164, W264 = m.U.f64, m.W1.f64, m.W2.f64
+    R, gamma, V = U64.shape
+    prev = m.anchor.astype(np.int64)
+    flagged = 0
+    for k in range(gamma):
+        Lref, _, _, _ = oracle.markov_step(U64[:, k], W164, W264, prev, m.uniforms[:, k], max(T, 1.0))
+        # float32 accumulation of rank products of bf16 values plus one rounding of U + bias
+        bound = 1e-6 * (1.0 + np.abs(Lref)) + (np.abs(Lref) * 2.0 ** -8 if logits_dtype == "bf16" else 0.0)
+        assert (np.abs(L[:, k] - Lref) <= bound).all(), f"step {k}: logits differ"
+        for r in range(R):
+            y = int(toks[r, k])
+            Lr = L[r, k] if logits_dtype == "bf16" else Lref[r]
+            if T == 0.0:
+                g = int(np.argmax(Lref[r]))
+                if y != g:
+                    srt = np.sort(Lref[r])
+                    assert Lref[r, y] >= srt[-1] - 2e-6 * (1 + abs(srt[-1])), "argmax differs beyond a near tie"
+                    flagged += 1
+                continue
+            pr = oracle.softmax_t(Lr, T)
+            C = np.cumsum(pr)
+            S = C[-1]
+            uu = float(m.uniforms[r, k])
+            lo = (C[y - 1] if y > 0 else 0.0) / S
+            hi = C[y] / S
+            assert pr[y] > 0 and lo - TOL <= uu < hi + TOL, f"step {k} request {r}: token {y} outside CDF bracket"
+            t_or, _, _ = oracle.inverse_cdf(pr, np.array(uu))
+            if int(t_or) != y:
+                flagged += 1
+        prev = toks[:, k].astype(np.int64)
+    return toks, flagged
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_markov_small(lib, T):
+    m = synth.markov(seed=301, R=37, gamma=4, V=1000, rank=64, temperature=T, w_scale=0.5)
+    _, flagged = _markov_check(lib, m, T)
+    assert flagged <= 3
+
+
+def test_markov_bf16_logits_and_rank256(lib):
+    m = synth.markov(seed=302, R=5, gamma=3, V=5000, rank=256, temperature=1.0, w_scale=0.3)
+    _markov_check(lib, m, 1.0, "bf16")
+
+
+def test_markov_long_vocab_single_request(lib):
+    """R=1, gamma=7, V=151936, rank 256, W ~ N(0, 0.02^2), T=1 and T=0."""
+    for T in (1.0, 0.0):
+        m = synth.markov(seed=2, temperature=T)
+        _markov_check(lib, m, T)
+
+
+def test_markov_large_batch_sampled_rows(lib):
+    """R=512, V=129280: the full DSpark drafting shape; every row's logits and tokens
+    are checked at each step (teacher-forced on the GPU's own tokens)."""
+    m = synth.markov(seed=5, R=512, gamma=7, V=129280)
+    sel = np.arange(0, 512, 37)
+    import torch
+    dev = torch.device("cuda")
+    toks, logits = lib.markov_draft(to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev),
+                                    to_torch(m.anchor, dev, np.int32), to_torch(m.uniforms, dev, np.float32), 1.0)
+    toks = toks.cpu().numpy()
+    L = logits[torch.from_numpy(sel).to(dev)].cpu().numpy().astype(np.float64)
+    U64, W164, W264 = m.U.f64[sel], m.W1.f64, m.W2.f64
+    prev = m.anchor[sel].astype(np.int64)
+    for k in range(7):
+        Lref, _, _, _ = oracle.markov_step(U64[:, k], W164, W264, prev, m.uniforms[sel, k], 1.0)
+        assert (np.abs(L[:, k] - Lref) <= 1e-6 * (1 + np.abs(Lref))).all()
+        for i, r in enumerate(sel):
+            pr = oracle.softmax_t(Lref[i], 1.0)
+            C = np.cumsum(pr)
+            y = int(toks[r, k])
+            uu = float(m.uniforms[r, k])
+            assert (C[y - 1] if y > 0 else 0.0) - TOL <= uu < C[y] + TOL
+        prev = toks[sel, k].astype(np.int64)
+
+
+# --------------------------------------------------------------------------- scheduler
+def _run_sched(lib, conf, sps, B_max=None):
+    import torch
+    dev = torch.device("cuda")
+    lengths, theta = lib.schedule(to_torch(conf, dev, np.float32), to_torch(sps, dev, np.float64), B_max)
+    return lengths.cpu().numpy(), float(theta.cpu().numpy()[0])
+
+
+@pytest.mark.parametrize("R,gamma", [(1, 1), (3, 3), (40, 7), (512, 7), (1000, 8), (8192, 1)])
+def test_schedule_matches_oracle(lib, R, gamma):
+    conf = synth.confidences(400 + R, R, gamma)
+    sps = synth.sps_table(max(4096, R * (gamma + 1)))
+    ell, theta = _run_sched(lib, conf, sps)
+    ref = oracle.schedule(conf, sps)
+    assert (ell == ref.lengths).all()
+    assert theta == ref.theta_best
+
+
+def test_schedule_special_tables(lib):
+    conf = synth.confidences(410, 64, 7)
+    ell, _ = _run_sched(lib, conf, np.full(4096, 5.0))
+    assert (ell == 7).all()
+    ell, _ = _run_sched(lib, conf, 1.0 / np.arange(1, 4097, dtype=np.float64) ** 2)
+    assert (ell == 0).all()
+    sps = np.array([10.0, 10.0, 10.0, 7.0, 9.0, 9.0, 9.0, 9.0])
+    c = np.full((2, 3), 0.9, dtype=np.float32)
+    ell, _ = _run_sched(lib, c, sps)
+    assert list(ell) == list(oracle.schedule(c, sps).lengths) == [1, 0]
+    # ties and the batch cap
+    c = np.array([[1.0, 0.5], [1.0, 1.0]], dtype=np.float32)
+    for bmax in (3, 4, 5, 6):
+        ell, _ = _run_sched(lib, c, np.full(8, 1.0), bmax)
+        assert list(ell) == list(oracle.schedule(c, np.full(8, 1.0), bmax).lengths)
+
+
+def test_schedule_bad_confidence(lib):
+    import torch
+    conf = synth.confidences(411, 8, 3)
+    conf[3, 1] = 1.5
+    dev = torch.device("cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    lengths, _ = lib.schedule(to_torch(conf, dev, np.float32), to_torch(synth.sps_table(64), dev, np.float64),
+                              workspace=ws)
+    assert (lengths.cpu().numpy() == -1).all()
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
