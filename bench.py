@@ -310,6 +310,7 @@ def run_ours(args):
 
 
 def main():
+    global R, ALGO_BYTES, WORKLOAD
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -318,9 +319,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--requests", type=int, default=R, help="R (smaller for profiling captures)")
+    ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     args = ap.parse_args()
-    global R, ALGO_BYTES, WORKLOAD
     if args.requests != R:
         R = args.requests
         ALGO_BYTES = R * (GAMMA + 1) * V * 2 + R * GAMMA * V * 2

@@ -31,18 +31,18 @@
 #include "common.cuh"
 #include "host_common.h"
 
+#include <atomic>
+
 namespace specv {
 
 constexpr int kStatsWarps = 8;        // warps (tiles) per CTA in chain_stats
 constexpr int kMaxCluster = 16;
 constexpr int kMaxTiles = kStatsWarps * kMaxCluster;   // 128 tiles per row
-constexpr int kFinishThreads = 128;
+constexpr int kFinishThreads = 256;
 constexpr int kArgmaxWarps = 8;
 
 struct RowRec {
   RowStats s;
-  float thr;        // min(1, q(x)/p(x)); NaN if the draft token is out of range
-  float pad[3];
 };
 
 struct StatsArgs {
@@ -64,10 +64,24 @@ struct StatsArgs {
 };
 
 // ---------------------------------------------------------------------------
-template <typename Elem, bool VEC, int VPT>
-__global__ void __launch_bounds__(kStatsWarps * 32, 2) chain_stats_kernel(StatsArgs a) {
+// Shared-memory layout of the target row's exponentials: for warp w, slot j,
+// half h (elements 4h .. 4h+3 of the slot) lane l's float4 sits at
+// [(w * VPT + j) * 2 + h][l], so a warp's 128-bit stores and loads are
+// contiguous (conflict-free).  Only the 16-byte path keeps them (VW == 8 or 4).
+//
+// NW warps per CTA (8 or 16).  KEEP_P: the draft row's float32 exponentials stay
+// in registers for pass 2; otherwise pass 2 recomputes them from the raw logits
+// (fewer registers, so 16-warp CTAs fit two per SM).
+template <typename Elem, bool VEC, int VPT, int NW, bool KEEP_P>
+__global__ void __launch_bounds__(NW * 32, 2) chain_stats_kernel(StatsArgs a) {
   using S = Slot<Elem, VEC>;
   constexpr int VW = S::VW;
+  constexpr int NE = VPT * VW;                 // elements per lane per row
+  constexpr int H = VW / 4;                    // float4 per slot (16-byte path)
+  extern __shared__ float4 s_exp[];            // target exponentials (16-byte path)
+  __shared__ float4 s_warp[NW];
+  __shared__ float4 s_cta;
+
   const uint32_t C = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int item = blockIdx.x / C;
@@ -88,148 +102,423 @@ __global__ void __launch_bounds__(kStatsWarps * 32, 2) chain_stats_kernel(StatsA
 
   const Elem* trow = reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * a.V;
   const Elem* drow = pair ? reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + k) * a.V : nullptr;
-  const int tile = int(rank) * kStatsWarps + warp;
+  const int tile = int(rank) * NW + warp;
   const bool active = tile < a.nwt;
 
-  // the draft token's logits for the accept test, fetched early
-  float lq_x = 0.f, lp_x = 0.f;
-  bool x_ok = false;
-  if (pair && a.tokens && rank == 0 && threadIdx.x == 0) {
-    const int x = a.tokens[size_t(r) * a.gamma + k];
-    x_ok = x >= 0 && x < a.V;
-    if (x_ok) {
-      if constexpr (sizeof(Elem) == 2) {
-        lq_x = __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(trow) + x)) << 16);
-        lp_x = __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(drow) + x)) << 16);
-      } else {
-        lq_x = __ldg(reinterpret_cast<const float*>(trow) + x);
-        lp_x = __ldg(reinterpret_cast<const float*>(drow) + x);
-      }
-    }
-  }
-
   S tq[VPT], tp[VPT];
-  if (active) {
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) tq[j].load(trow, slot_index<VPT, VW>(tile, j, lane), a.V);
-    if (pair) {
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) tp[j].load(drow, slot_index<VPT, VW>(tile, j, lane), a.V);
-    }
+  for (int j = 0; j < VPT; ++j) {
+    if (active) tq[j].load(trow, slot_index<VPT, VW>(tile, j, lane), a.V);
+    else tq[j].set_neg_inf();
   }
+  auto load_draft = [&]() {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      if (active && pair) tp[j].load(drow, slot_index<VPT, VW>(tile, j, lane), a.V);
+      else tp[j].set_neg_inf();
+    }
+  };
+  // with the draft exponentials kept in registers both rows are in flight at once;
+  // otherwise the draft row is fetched after the target row's registers are free
+  if constexpr (KEEP_P) load_draft();
 
-  // ---- pass 1: tile max and tile normaliser (ex2 domain)
   const float c2 = a.c2;
-  float mq = neg_inf(), mp = neg_inf();
-  if (active) {
+  // ---- pass 1, target row: tile max, exponentials (kept in shared memory), tile normaliser
+  float mq = neg_inf();
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) mq = fmaxf(mq, tq[j].vmax());
-    if (pair) {
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) mp = fmaxf(mp, tp[j].vmax());
-    }
-  }
+  for (int j = 0; j < VPT; ++j) mq = fmaxf(mq, tq[j].vmax());
   mq = warp_max(mq);
-  mp = warp_max(mp);
   const bool q_live = mq > neg_inf();
-  const bool p_live = mp > neg_inf();
-  const float mq_c2 = q_live ? mq * c2 : neg_inf();
-  const float mp_c2 = p_live ? mp * c2 : neg_inf();
-  float zq = 0.f, zp = 0.f;
+  const float mq_c2 = q_live ? mq * c2 : 0.f;
+  float zq = 0.f;
+  float eq_reg[VEC ? 1 : NE];                    // unaligned path keeps them in registers
   if (q_live) {
+    float2 za = make_float2(0.f, 0.f), zb = make_float2(0.f, 0.f);   // independent chains
 #pragma unroll
-    for (int j = 0; j < VPT; ++j)
+    for (int j = 0; j < VPT; ++j) {
+      if constexpr (VEC) {
 #pragma unroll
-      for (int e = 0; e < VW; ++e) zq += ex2(fmaf(tq[j].get(e), c2, -mq_c2));
-  }
-  if (p_live) {
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-#pragma unroll
-      for (int e = 0; e < VW; ++e) zp += ex2(fmaf(tp[j].get(e), c2, -mp_c2));
-  }
-  zq = warp_sum(zq);
-  zp = warp_sum(zp);
-
-  // ---- cluster exchange of tile partials
-  __shared__ float4 s_tiles[kStatsWarps];
-  __shared__ float4 s_row;
-  if (lane == 0) s_tiles[warp] = make_float4(mq_c2, zq, mp_c2, zp);
-  cluster_arrive_release();
-  cluster_wait_acquire();
-  if (warp == 0) {
-    const int ntile = int(C) * kStatsWarps;
-    float4 t[kMaxTiles / 32];
-    float Mq = neg_inf(), Mp = neg_inf();
-#pragma unroll
-    for (int i = 0; i < kMaxTiles / 32; ++i) {
-      const int tt = lane + 32 * i;
-      if (tt < ntile) {
-        t[i] = ld_shared_cluster_f4(cluster_map_shared(&s_tiles[tt % kStatsWarps], uint32_t(tt / kStatsWarps)));
+        for (int h = 0; h < H; ++h) {
+          const float2 t0 = fma2(make_float2(tq[j].get(4 * h), tq[j].get(4 * h + 1)), make_float2(c2, c2),
+                                 make_float2(-mq_c2, -mq_c2));
+          const float2 t1 = fma2(make_float2(tq[j].get(4 * h + 2), tq[j].get(4 * h + 3)), make_float2(c2, c2),
+                                 make_float2(-mq_c2, -mq_c2));
+          const float4 e = make_float4(ex2(t0.x), ex2(t0.y), ex2(t1.x), ex2(t1.y));
+          za = add2(za, make_float2(e.x, e.y));
+          zb = add2(zb, make_float2(e.z, e.w));
+          s_exp[((warp * VPT + j) * H + h) * 32 + lane] = e;
+        }
       } else {
-        t[i] = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+        const float e = ex2(fmaf(tq[j].get(0), c2, -mq_c2));
+        eq_reg[j] = e;
+        if (j & 1) zb.x += e; else za.x += e;
       }
-      Mq = fmaxf(Mq, t[i].x);
-      Mp = fmaxf(Mp, t[i].z);
     }
-    Mq = warp_max(Mq);
-    Mp = warp_max(Mp);
-    float Zq = 0.f, Zp = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxTiles / 32; ++i) {
-      if (t[i].y > 0.f) Zq += t[i].y * ex2(t[i].x - Mq);
-      if (t[i].w > 0.f) Zp += t[i].w * ex2(t[i].z - Mp);
-    }
-    Zq = warp_sum(Zq);
-    Zp = warp_sum(Zp);
-    if (lane == 0) s_row = make_float4(Mq, Zq, Mp, Zp);
+    zq = warp_sum((za.x + za.y) + (zb.x + zb.y));
   }
-  cluster_arrive_relaxed();            // remote shared-memory reads of this CTA are done
-  __syncthreads();
-  const float4 row = s_row;
 
-  // ---- pass 2: tile residual mass and q mass
-  const float sq = q_live ? tile_scale(mq_c2, row.x, row.y) : 0.f;
-  const float sp = p_live ? tile_scale(mp_c2, row.z, row.w) : 0.f;
+  // ---- pass 1, draft row
+  if constexpr (!KEEP_P) {
+    asm volatile("" ::: "memory");
+    load_draft();
+  }
+  float mp = neg_inf();
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) mp = fmaxf(mp, tp[j].vmax());
+  mp = warp_max(mp);
+  const bool p_live = mp > neg_inf();
+  const float mp_c2 = p_live ? mp * c2 : 0.f;
+  // masked elements are -inf, so their exponentials are 0 without a select
+  float ep[KEEP_P ? NE : 2];
+  float zp = 0.f;
+  {
+    float2 za = make_float2(0.f, 0.f), zb = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int e = 0; e < VW; e += (VW > 1 ? 2 : 1)) {
+        if constexpr (VW > 1) {
+          const float2 t = fma2(make_float2(tp[j].get(e), tp[j].get(e + 1)), make_float2(c2, c2),
+                                make_float2(-mp_c2, -mp_c2));
+          const float2 pe = make_float2(ex2(t.x), ex2(t.y));
+          if constexpr (KEEP_P) {
+            ep[j * VW + e] = pe.x;
+            ep[j * VW + e + 1] = pe.y;
+          }
+          if ((e >> 1) & 1) zb = add2(zb, pe);
+          else za = add2(za, pe);
+        } else {
+          const float pe = ex2(fmaf(tp[j].get(0), c2, -mp_c2));
+          if constexpr (KEEP_P) ep[j] = pe;
+          if (j & 1) zb.x += pe; else za.x += pe;
+        }
+      }
+    if (p_live) zp = warp_sum((za.x + za.y) + (zb.x + zb.y));
+  }
+
+  // ---- CTA partial, then the row statistics across the cluster (distributed shared memory)
+  if (lane == 0) s_warp[warp] = make_float4(q_live ? mq_c2 : neg_inf(), zq, p_live ? mp_c2 : neg_inf(), zp);
+  __syncthreads();
+  if (warp == 0) {
+    const float4 w = lane < NW ? s_warp[lane] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+    const float Mq = warp_max(w.x), Mp = warp_max(w.z);
+    const float Zq = warp_sum(w.y > 0.f ? w.y * ex2(w.x - Mq) : 0.f);
+    const float Zp = warp_sum(w.w > 0.f ? w.w * ex2(w.z - Mp) : 0.f);
+    if (lane == 0) s_cta = make_float4(Mq, Zq, Mp, Zp);
+    cluster_arrive_release();            // publishes s_cta to the cluster
+  } else {
+    cluster_arrive_relaxed();
+  }
+  cluster_wait_acquire();
+  const float4 cp = lane < int(C) ? ld_shared_cluster_f4(cluster_map_shared(&s_cta, uint32_t(lane)))
+                                  : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+  const float Mq = warp_max(cp.x), Mp = warp_max(cp.z);
+  const float Zq = warp_sum(cp.y > 0.f ? cp.y * ex2(cp.x - Mq) : 0.f);
+  const float Zp = warp_sum(cp.w > 0.f ? cp.w * ex2(cp.z - Mp) : 0.f);
+  cluster_arrive_relaxed();              // this CTA's remote reads are done
+
+  // ---- pass 2: tile residual mass sum [q - p]_+ = Q_tile - sum min(q, p), no second
+  // exponential.  min(sq*eq, sp*ep) = s_hi * min(e_hi, rho * e_lo) with rho <= 1.
+  const float sq = q_live ? tile_scale(mq_c2, Mq, Zq) : 0.f;
+  const float sp = p_live ? tile_scale(mp_c2, Mp, Zp) : 0.f;
   float resid = 0.f;
   if (pair && q_live) {
+    const bool q_hi = sq >= sp;
+    const float rho = q_hi ? sp / sq : sq / sp;
+    float2 aa = make_float2(0.f, 0.f), ab = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < VPT; ++j)
+    for (int j = 0; j < VPT; ++j) {
+      if constexpr (VEC) {
 #pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        const float eq = ex2(fmaf(tq[j].get(e), c2, -mq_c2));
-        const float ep = p_live ? ex2(fmaf(tp[j].get(e), c2, -mp_c2)) : 0.f;
-        resid += fmaxf(fmaf(eq, sq, -__fmul_rn(ep, sp)), 0.f);
+        for (int h = 0; h < H; ++h) {
+          const float4 e = s_exp[((warp * VPT + j) * H + h) * 32 + lane];
+          float2 q0 = make_float2(e.x, e.y), q1 = make_float2(e.z, e.w);
+          float2 p0, p1;
+          if constexpr (KEEP_P) {
+            const float* pe = ep + j * VW + 4 * h;
+            p0 = make_float2(pe[0], pe[1]);
+            p1 = make_float2(pe[2], pe[3]);
+          } else {
+            const float2 t0 = fma2(make_float2(tp[j].get(4 * h), tp[j].get(4 * h + 1)), make_float2(c2, c2),
+                                   make_float2(-mp_c2, -mp_c2));
+            const float2 t1 = fma2(make_float2(tp[j].get(4 * h + 2), tp[j].get(4 * h + 3)), make_float2(c2, c2),
+                                   make_float2(-mp_c2, -mp_c2));
+            p0 = make_float2(ex2(t0.x), ex2(t0.y));
+            p1 = make_float2(ex2(t1.x), ex2(t1.y));
+          }
+          if (q_hi) {
+            p0 = mul2(p0, make_float2(rho, rho));
+            p1 = mul2(p1, make_float2(rho, rho));
+          } else {
+            q0 = mul2(q0, make_float2(rho, rho));
+            q1 = mul2(q1, make_float2(rho, rho));
+          }
+          aa = add2(aa, make_float2(fminf(q0.x, p0.x), fminf(q0.y, p0.y)));
+          ab = add2(ab, make_float2(fminf(q1.x, p1.x), fminf(q1.y, p1.y)));
+        }
+      } else {
+        float epj;
+        if constexpr (KEEP_P) epj = ep[j];
+        else epj = ex2(fmaf(tp[j].get(0), c2, -mp_c2));
+        const float qv = q_hi ? eq_reg[j] : eq_reg[j] * rho;
+        const float pv = q_hi ? epj * rho : epj;
+        if (j & 1) ab.x += fminf(qv, pv); else aa.x += fminf(qv, pv);
       }
+    }
+    const float mins = warp_sum((aa.x + aa.y) + (ab.x + ab.y)) * (q_hi ? sq : sp);
+    resid = fmaxf(__fmul_rn(sq, zq) - mins, 0.f);
   }
-  resid = warp_sum(resid);
   if (lane == 0 && active) {
     TileStats ts;
-    ts.mq_c2 = mq_c2;
-    ts.mp_c2 = mp_c2;
+    ts.mq_c2 = q_live ? mq_c2 : neg_inf();
+    ts.mp_c2 = p_live ? mp_c2 : neg_inf();
     ts.resid = resid;
     ts.qmass = __fmul_rn(sq, zq);
     a.tiles[size_t(item) * a.ntile_stride + tile] = ts;
   }
   if (rank == 0 && threadIdx.x == 0) {
     RowRec rr;
-    rr.s.Mq_c2 = row.x; rr.s.Zq = row.y; rr.s.Mp_c2 = row.z; rr.s.Zp = row.w;
-    rr.thr = __int_as_float(0x7fc00000);
-    if (pair && a.tokens && x_ok) {
-      const float qx = ex2(fmaf(lq_x, c2, -row.x)) / row.y;
-      const float px = ex2(fmaf(lp_x, c2, -row.z)) / row.w;
-      rr.thr = px > 0.f ? fminf(1.f, qx / px) : 1.f;
-    }
-    rr.pad[0] = rr.pad[1] = rr.pad[2] = 0.f;
+    rr.s.Mq_c2 = Mq; rr.s.Zq = Zq; rr.s.Mp_c2 = Mp; rr.s.Zp = Zp;
     a.rows[item] = rr;
   }
   cluster_wait_acquire();              // keep shared memory alive until every CTA has read it
 }
 
 // ---------------------------------------------------------------------------
+// chain_stats, persistent and pipelined form for 16-byte-aligned rows.
+//
+// A grid of 8-CTA clusters sized to what fits at once (two 8-warp CTAs per
+// SM); cluster c handles items c, c + n_clusters, ...  Every thread owns the
+// same VPT slots of its warp tile in each row, and prefetches its slots of the
+// next item into a private area of shared memory with 16-byte cp.async copies
+// while the current item is processed from registers (no block-wide sync is
+// needed for the staging: a thread only reads what it copied).  Pass 2
+// recomputes the exponentials from the registers.  Tile partials are
+// exchanged through distributed shared memory, double-buffered by the parity of
+// the processed-item count so that one cluster barrier per item suffices.
+struct PipeArgs {
+  StatsArgs s;
+  int items;        // R * P
+  int ncl;          // clusters in the grid
+};
+
+template <typename Elem, int VPT, int NW>
+__global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs pa) {
+  using S = Slot<Elem, true>;
+  constexpr int VW = S::VW;
+  const StatsArgs& a = pa.s;
+  extern __shared__ uint4 s_stage[];            // [2 rows][VPT][threads]
+  __shared__ float4 s_warp[2][NW];
+  __shared__ float4 s_cta[2];
+
+  const uint32_t C = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int cid = blockIdx.x / C;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = int(rank) * NW + warp;
+  const bool active = tile < a.nwt;
+  const long V = a.V;
+  const float c2 = a.c2;
+  if (cid == 0 && rank == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
+
+  auto decode = [&](int item, int& r, int& k) -> int {   // 0 skip, 1 row pair, 2 bonus row
+    r = item / a.P;
+    k = item - r * a.P;
+    int ell = a.gamma;
+    if (a.lengths) {
+      ell = __ldg(a.lengths + r);
+      if (ell < 0 || ell > a.gamma) return 0;
+    }
+    if (k < ell) return 1;
+    return (a.with_bonus && k == ell) ? 2 : 0;
+  };
+  auto stage = [&](int row, int j) -> uint4* { return s_stage + (row * VPT + j) * (NW * 32) + threadIdx.x; };
+  auto prefetch = [&](int item) {
+    if (item >= pa.items || !active) return;
+    int r, k;
+    const int kind = decode(item, r, k);
+    if (kind == 0) return;
+    const Elem* trow = reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * size_t(V);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const long idx = slot_index<VPT, VW>(tile, j, lane);
+      if (idx < V) cp_async16(stage(0, j), trow + idx);
+    }
+    if (kind == 1) {
+      const Elem* drow = reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + k) * size_t(V);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const long idx = slot_index<VPT, VW>(tile, j, lane);
+        if (idx < V) cp_async16(stage(1, j), drow + idx);
+      }
+    }
+  };
+
+  prefetch(cid);
+  cp_async_commit();
+  int processed = 0;
+  for (int n = 0;; ++n) {
+    const int item = cid + n * pa.ncl;
+    if (item >= pa.items) break;
+    int r, k;
+    const int kind = decode(item, r, k);
+    cp_async_wait_all();                         // this thread's copies of `item` have landed
+    S tq[VPT], tp[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const bool in = kind != 0 && active && slot_index<VPT, VW>(tile, j, lane) < V;
+      if (in) {
+        const uint4 v = *stage(0, j);
+        tq[j].w[0] = v.x; tq[j].w[1] = v.y; tq[j].w[2] = v.z; tq[j].w[3] = v.w;
+      } else {
+        tq[j].set_neg_inf();
+      }
+      if (in && kind == 1) {
+        const uint4 v = *stage(1, j);
+        tp[j].w[0] = v.x; tp[j].w[1] = v.y; tp[j].w[2] = v.z; tp[j].w[3] = v.w;
+      } else {
+        tp[j].set_neg_inf();
+      }
+    }
+    // tile maxima: consumes every staged value, so the slots are free to refill
+    float mq = neg_inf(), mp = neg_inf();
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      mq = fmaxf(mq, tq[j].vmax());
+      mp = fmaxf(mp, tp[j].vmax());
+    }
+    prefetch(cid + (n + 1) * pa.ncl);
+    cp_async_commit();
+    if (kind == 0) continue;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+      mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+    }
+    const bool q_live = mq > neg_inf();
+    const bool p_live = mp > neg_inf();
+    const float mq_c2 = q_live ? mq * c2 : 0.f;
+    const float mp_c2 = p_live ? mp * c2 : 0.f;
+
+    // ---- pass 1: tile normalisers for both rows (masked elements are -inf -> 0)
+    auto tile_sum = [&](const S* x, float m_c2) -> float {
+      float2 za = make_float2(0.f, 0.f), zb = za;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int e = 0; e < VW; e += 4) {
+          const float2 t0 = fma2(make_float2(x[j].get(e), x[j].get(e + 1)), make_float2(c2, c2), make_float2(-m_c2, -m_c2));
+          za = add2(za, make_float2(ex2(t0.x), ex2(t0.y)));
+          const float2 t1 = fma2(make_float2(x[j].get(e + 2), x[j].get(e + 3)), make_float2(c2, c2), make_float2(-m_c2, -m_c2));
+          zb = add2(zb, make_float2(ex2(t1.x), ex2(t1.y)));
+        }
+      return (za.x + za.y) + (zb.x + zb.y);
+    };
+    float zq = tile_sum(tq, mq_c2);
+    float zp = tile_sum(tp, mp_c2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zq += __shfl_xor_sync(0xffffffffu, zq, o);
+      zp += __shfl_xor_sync(0xffffffffu, zp, o);
+    }
+    if (!q_live) zq = 0.f;
+    if (!p_live) zp = 0.f;
+
+    // ---- CTA partial, then the cluster-wide row statistics
+    const int pb = processed & 1;
+    if (lane == 0) s_warp[pb][warp] = make_float4(q_live ? mq_c2 : neg_inf(), zq, p_live ? mp_c2 : neg_inf(), zp);
+    __syncthreads();
+    if (warp == 0) {
+      const float4 w = lane < NW ? s_warp[pb][lane] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+      float Mq = w.x, Mp = w.z;
+#pragma unroll
+      for (int o = NW / 2; o > 0; o >>= 1) {
+        Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, o));
+        Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, o));
+      }
+      float Zq = w.y > 0.f ? w.y * ex2(w.x - Mq) : 0.f;
+      float Zp = w.w > 0.f ? w.w * ex2(w.z - Mp) : 0.f;
+#pragma unroll
+      for (int o = NW / 2; o > 0; o >>= 1) {
+        Zq += __shfl_xor_sync(0xffffffffu, Zq, o);
+        Zp += __shfl_xor_sync(0xffffffffu, Zp, o);
+      }
+      if (lane == 0) s_cta[pb] = make_float4(Mq, Zq, Mp, Zp);
+      cluster_arrive_release();
+    } else {
+      cluster_arrive_relaxed();
+    }
+    cluster_wait_acquire();
+    const float4 cc = lane < int(C) ? ld_shared_cluster_f4(cluster_map_shared(&s_cta[pb], uint32_t(lane)))
+                                    : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+    float Mq = cc.x, Mp = cc.z;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {             // every lane needs the row statistics
+      Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, o));
+      Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, o));
+    }
+    float Zq = cc.y > 0.f ? cc.y * ex2(cc.x - Mq) : 0.f;
+    float Zp = cc.w > 0.f ? cc.w * ex2(cc.z - Mp) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Zq += __shfl_xor_sync(0xffffffffu, Zq, o);
+      Zp += __shfl_xor_sync(0xffffffffu, Zp, o);
+    }
+
+    // ---- pass 2: sum min(q, p) per tile with recomputed exponentials
+    const float sq = q_live ? tile_scale(mq_c2, Mq, Zq) : 0.f;
+    const float sp = p_live ? tile_scale(mp_c2, Mp, Zp) : 0.f;
+    float resid = 0.f;
+    if (kind == 1 && q_live) {
+      // min(q, p) = 2^min(x_q*c2 + lq, x_p*c2 + lp): one exponential per position
+      float lq, lp;
+      asm("lg2.approx.f32 %0, %1;" : "=f"(lq) : "f"(sq));
+      asm("lg2.approx.f32 %0, %1;" : "=f"(lp) : "f"(sp));
+      lq -= mq_c2;
+      lp = p_live ? lp - mp_c2 : neg_inf();
+      float2 ma = make_float2(0.f, 0.f), mb = ma;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int e = 0; e < VW; e += 2) {
+          const float2 t = fma2(make_float2(tq[j].get_fresh(e), tq[j].get_fresh(e + 1)), make_float2(c2, c2),
+                                make_float2(lq, lq));
+          const float2 u = fma2(make_float2(tp[j].get_fresh(e), tp[j].get_fresh(e + 1)), make_float2(c2, c2),
+                                make_float2(lp, lp));
+          const float2 mn = make_float2(ex2(fminf(t.x, u.x)), ex2(fminf(t.y, u.y)));
+          if ((e >> 1) & 1) mb = add2(mb, mn); else ma = add2(ma, mn);
+        }
+      float mins = (ma.x + ma.y) + (mb.x + mb.y);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mins += __shfl_xor_sync(0xffffffffu, mins, o);
+      resid = fmaxf(__fmul_rn(sq, zq) - mins, 0.f);
+    }
+    if (lane == 0 && active) {
+      TileStats ts;
+      ts.mq_c2 = q_live ? mq_c2 : neg_inf();
+      ts.mp_c2 = p_live ? mp_c2 : neg_inf();
+      ts.resid = resid;
+      ts.qmass = __fmul_rn(sq, zq);
+      a.tiles[size_t(item) * a.ntile_stride + tile] = ts;
+    }
+    if (rank == 0 && threadIdx.x == 0) {
+      RowRec rr;
+      rr.s.Mq_c2 = Mq; rr.s.Zq = Zq; rr.s.Mp_c2 = Mp; rr.s.Zp = Zp;
+      a.rows[item] = rr;
+    }
+    ++processed;
+  }
+  cp_async_wait_all();
+  cluster_arrive_release();            // no CTA leaves while another may still read its partials
+  cluster_wait_acquire();
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
 struct FinishArgs {
   const void* target;
   const void* draft;
+  const int32_t* tokens;      // [R, gamma]
   const int32_t* lengths;
   const float* uniforms;      // [R, gamma+1, 2]
   const RowRec* rows;
@@ -245,180 +534,250 @@ struct FinishArgs {
   int sample;                 // 0: c* only (tv_accept)
 };
 
-// Inverse-CDF draw inside one tile (one warp).  `use_resid`: weights
-// [q - p]_+ (else q).  Returns the first element index v with
-// base + C_tile(v) > target, or, if rounding leaves none, the last element with
-// positive weight.  Same per-element arithmetic as chain_stats pass 2.
-template <typename Elem, bool VEC, int VPT>
-__device__ int rescan_tile(const Elem* trow, const Elem* drow, long V, int tile, float c2, const TileStats& ts,
-                           const RowStats& rs, bool use_resid, float base, float target) {
-  using S = Slot<Elem, VEC>;
-  constexpr int VW = S::VW;
-  const int lane = threadIdx.x & 31;
-  const bool q_live = ts.mq_c2 > neg_inf();
-  const bool p_live = use_resid && ts.mp_c2 > neg_inf();
-  const float sq = q_live ? tile_scale(ts.mq_c2, rs.Mq_c2, rs.Zq) : 0.f;
-  const float sp = p_live ? tile_scale(ts.mp_c2, rs.Mp_c2, rs.Zp) : 0.f;
-  float run = base;
-  int last_pos = -1;
-  for (int j = 0; j < VPT; ++j) {
-    const long idx0 = slot_index<VPT, VW>(tile, j, lane);
-    S xq, xp;
-    xq.load(trow, idx0, V);
-    if (use_resid) xp.load(drow, idx0, V);
-    float w[VW];
-    float lsum = 0.f;
-#pragma unroll
-    for (int e = 0; e < VW; ++e) {
-      float we = 0.f;
-      if (q_live) {
-        const float eq = ex2(fmaf(xq.get(e), c2, -ts.mq_c2));
-        if (use_resid) {
-          const float ep = p_live ? ex2(fmaf(xp.get(e), c2, -ts.mp_c2)) : 0.f;
-          we = fmaxf(fmaf(eq, sq, -__fmul_rn(ep, sp)), 0.f);
-        } else {
-          we = __fmul_rn(eq, sq);
-        }
-      }
-      w[e] = we;
-      lsum += we;
-    }
-    const float incl = warp_inclusive_scan(lsum);
-    float acc = run + (incl - lsum);
-    int cand = 0x7fffffff;
-#pragma unroll
-    for (int e = 0; e < VW; ++e) {
-      acc += w[e];
-      if (w[e] > 0.f) last_pos = int(idx0) + e;
-      if (cand == 0x7fffffff && acc > target && w[e] > 0.f) cand = int(idx0) + e;
-    }
-    int best = cand;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
-    if (best != 0x7fffffff) return best;
-    run = __shfl_sync(0xffffffffu, acc, 31);
-  }
-  int lp = last_pos;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-  return lp;
+// Per-element weight of the inverse-CDF draw: [q - p]_+ (rejection) or q
+// (bonus), with the same arithmetic as chain_stats.
+template <typename S>
+__device__ __forceinline__ float draw_weight(const S& xq, const S& xp, int e, float c2, const TileStats& ts, float sq,
+                                             float sp, bool q_live, bool p_live, bool use_resid) {
+  if (!q_live) return 0.f;
+  const float eq = ex2(fmaf(xq.get(e), c2, -ts.mq_c2));
+  if (!use_resid) return __fmul_rn(eq, sq);
+  const float ep = p_live ? ex2(fmaf(xp.get(e), c2, -ts.mp_c2)) : 0.f;
+  return fmaxf(fmaf(eq, sq, -__fmul_rn(ep, sp)), 0.f);
 }
 
+// One CTA per request.  Phase 1, one warp per position k <= l_r in parallel:
+// c*_k, the accept threshold min(1, q(x_k)/p(x_k)), and the tile a draw at k
+// would come from (prefix over the tile masses: [q - p]_+ for k < l_r, q for
+// the bonus position).  Phase 2: warp 0 finds the first rejection A by ballot.
+// Phase 3: every warp rescans one slot of A's selected tile; a prefix over the
+// slot totals picks the slot, one warp scan inside it picks the token.
 template <typename Elem, bool VEC, int VPT>
 __global__ void __launch_bounds__(kFinishThreads) chain_finish_kernel(FinishArgs a) {
+  using S = Slot<Elem, VEC>;
+  constexpr int VW = S::VW;
+  constexpr int NWARP = kFinishThreads / 32;
+  __shared__ float s_thr[SPECV_MAX_GAMMA + 1];
+  __shared__ int s_sel[SPECV_MAX_GAMMA + 1];       // selected tile (-1: none)
+  __shared__ float s_base[SPECV_MAX_GAMMA + 1];    // mass before that tile
+  __shared__ float s_target[SPECV_MAX_GAMMA + 1];  // u * total mass
+  __shared__ int s_resid[SPECV_MAX_GAMMA + 1];     // draw from [q-p]_+ (1) or q (0)
+  __shared__ float s_slot[VPT];
+  __shared__ int s_slot_last[VPT];
+  __shared__ int s_bad, s_A, s_tok;
+  pdl_wait_primary();
   const int r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gamma = a.gamma;
-  int ell = a.lengths ? a.lengths[r] : gamma;
-  bool bad = ell < 0 || ell > gamma;
-  if (bad) ell = 0;
+  int ell = a.lengths ? __ldg(a.lengths + r) : gamma;
+  const bool bad_len = ell < 0 || ell > gamma;
+  if (bad_len) ell = 0;
+  if (threadIdx.x == 0) {
+    s_bad = bad_len ? 1 : 0;
+    s_tok = -1;
+  }
+  __syncthreads();
 
-  // ---- c*_k = 1 - sum of tile residual masses
-  if (a.c_star) {
-    for (int k = warp; k < gamma; k += kFinishThreads / 32) {
-      float c = __int_as_float(0x7fc00000);
-      if (!bad && k < ell) {
-        const TileStats* ts = a.tiles + size_t(r * a.P + k) * a.ntile_stride;
-        float s = 0.f;
-        for (int t = lane; t < a.nwt; t += 32) s += ts[t].resid;
-        s = warp_sum(s);
-        c = 1.f - s;
+  // ---- phase 1
+  const int kmax = a.sample ? ell : ell - 1;
+  for (int k = warp; k <= kmax && !bad_len; k += NWARP) {
+    const int item = r * a.P + k;
+    const TileStats* ts = a.tiles + size_t(item) * a.ntile_stride;
+    const bool pair = k < ell;
+    const int per = (a.nwt + 31) / 32;            // consecutive tiles per lane (index order), <= 4
+    const int t0 = lane * per, t1 = min(a.nwt, t0 + per);
+    float tres[kMaxTiles / 32], tqm[kMaxTiles / 32];
+    float rsum = 0.f, qsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxTiles / 32; ++i) {
+      tres[i] = 0.f;
+      tqm[i] = 0.f;
+      if (t0 + i < t1) {
+        const TileStats x = ts[t0 + i];
+        tres[i] = x.resid;
+        tqm[i] = x.qmass;
       }
-      if (lane == 0) a.c_star[size_t(r) * gamma + k] = c;
+      rsum += tres[i];
+      qsum += tqm[i];
     }
-  }
-  if (!a.sample || warp != 0) return;
-
-  // ---- first rejection (warp ballot over the accept tests)
-  bool acc_ok = true, valid = true;
-  if (lane < ell) {
-    const float thr = a.rows[r * a.P + lane].thr;
-    const float u0 = a.uniforms[(size_t(r) * (gamma + 1) + lane) * 2];
-    valid = !isnan(thr) && u0 >= 0.f && u0 < 1.f;
-    acc_ok = u0 < thr;
-  }
-  bad = bad || __any_sync(0xffffffffu, !valid);
-  const unsigned rej = __ballot_sync(0xffffffffu, !acc_ok) & (ell >= 32 ? 0xffffffffu : ((1u << ell) - 1u));
-  const int A = rej ? __ffs(rej) - 1 : ell;
-  const float u1 = a.uniforms[(size_t(r) * (gamma + 1) + A) * 2 + 1];
-  bad = bad || !(u1 >= 0.f && u1 < 1.f);
-  if (bad) {
+    int x = 0;
+    float u0 = 0.f, u1 = 0.f;
+    if (a.sample) {
+      if (pair) x = __ldg(a.tokens + size_t(r) * gamma + k);
+      u0 = __ldg(a.uniforms + (size_t(r) * (gamma + 1) + k) * 2);
+      u1 = __ldg(a.uniforms + (size_t(r) * (gamma + 1) + k) * 2 + 1);
+    }
+    const float resid_total = warp_sum(rsum);
+    if (pair && a.c_star && lane == 0) a.c_star[size_t(r) * gamma + k] = 1.f - resid_total;
+    if (!a.sample) continue;
+    const bool bad = !(u1 >= 0.f && u1 < 1.f) || (pair && !(u0 >= 0.f && u0 < 1.f)) || (pair && !(x >= 0 && x < a.V));
+    // the tile a draw at k comes from
+    bool use_resid = pair;
+    float lsum = use_resid ? rsum : qsum;
+    float incl = warp_inclusive_scan(lsum);
+    float total = __shfl_sync(0xffffffffu, incl, 31);
+    if (use_resid && !(total > 0.f)) {            // no residual mass: draw from q
+      use_resid = false;
+      lsum = qsum;
+      incl = warp_inclusive_scan(lsum);
+      total = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    const float target = u1 * total;
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > target && t1 > t0);
+    int sel_tile = -1;
+    float base = 0.f;
+    {
+      const int L = hit ? __ffs(hit) - 1 : 31;
+      if (lane == L) {
+        // first tile of this lane whose running sum passes the target; if rounding
+        // leaves none, the lane's last tile with mass
+        float run = incl - lsum;
+        bool found = false;
+#pragma unroll
+        for (int i = 0; i < kMaxTiles / 32; ++i) {
+          const float m = use_resid ? tres[i] : tqm[i];
+          if (!found && t0 + i < t1 && m > 0.f) {
+            sel_tile = t0 + i;
+            base = run;
+            found = hit && run + m > target;
+          }
+          if (!found) run += m;
+        }
+      }
+      sel_tile = __shfl_sync(0xffffffffu, sel_tile, L);
+      base = __shfl_sync(0xffffffffu, base, L);
+    }
+    // accept threshold from the draft token's two logits
+    float thr = 1.f;
+    if (pair && !bad && lane == 0) {
+      const RowStats rs = a.rows[item].s;
+      const size_t iq = (size_t(r) * a.Pt + k) * size_t(a.V) + x;
+      const size_t ip = (size_t(r) * a.Pd + k) * size_t(a.V) + x;
+      float lq, lp;
+      if constexpr (sizeof(Elem) == 2) {
+        lq = __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(a.target) + iq)) << 16);
+        lp = __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(a.draft) + ip)) << 16);
+      } else {
+        lq = __ldg(reinterpret_cast<const float*>(a.target) + iq);
+        lp = __ldg(reinterpret_cast<const float*>(a.draft) + ip);
+      }
+      const float qx = ex2(fmaf(lq, a.c2, -rs.Mq_c2)) / rs.Zq;
+      const float px = ex2(fmaf(lp, a.c2, -rs.Mp_c2)) / rs.Zp;
+      thr = px > 0.f ? fminf(1.f, qx / px) : 1.f;
+    }
     if (lane == 0) {
-      a.accepted[r] = -1;
-      a.out_token[r] = -1;
-      record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
+      s_thr[k] = thr;
+      s_sel[k] = sel_tile;
+      s_base[k] = base;
+      s_target[k] = target;
+      s_resid[k] = use_resid ? 1 : 0;
+      if (bad) s_bad = 1;
     }
-    return;
   }
+  if (a.c_star && lane == 0)
+    for (int k = warp; k < gamma; k += NWARP)
+      if (bad_len || k >= ell) a.c_star[size_t(r) * gamma + k] = __int_as_float(0x7fc00000);
+  if (!a.sample) return;
+  __syncthreads();
 
-  // ---- inverse-CDF draw: residual of position A (rejection) or q at l_r (bonus)
-  const int item = r * a.P + A;
-  const TileStats* ts = a.tiles + size_t(item) * a.ntile_stride;
-  const RowStats rs = a.rows[item].s;
-  bool use_resid = A < ell;
-  const int per = (a.nwt + 31) / 32;          // consecutive tiles per lane (index order)
-  const int t0 = lane * per, t1 = min(a.nwt, t0 + per);
-  float lsum = 0.f;
-  for (int t = t0; t < t1; ++t) lsum += use_resid ? ts[t].resid : ts[t].qmass;
-  float incl = warp_inclusive_scan(lsum);
-  float total = __shfl_sync(0xffffffffu, incl, 31);
-  if (use_resid && !(total > 0.f)) {          // no residual mass: draw from q
-    use_resid = false;
-    lsum = 0.f;
-    for (int t = t0; t < t1; ++t) lsum += ts[t].qmass;
-    incl = warp_inclusive_scan(lsum);
-    total = __shfl_sync(0xffffffffu, incl, 31);
+  // ---- phase 2: first rejection
+  if (warp == 0) {
+    bool rej = false;
+    if (!bad_len && lane < ell) {
+      const float u0 = __ldg(a.uniforms + (size_t(r) * (gamma + 1) + lane) * 2);
+      rej = !(u0 < s_thr[lane]);
+    }
+    const unsigned rm = __ballot_sync(0xffffffffu, rej);
+    if (lane == 0) s_A = rm ? __ffs(rm) - 1 : ell;
   }
-  const float target = u1 * total;
-  // the tile holding the target: first lane whose range crosses it, then its tiles in order
-  const unsigned hit = __ballot_sync(0xffffffffu, incl > target && t1 > t0);
-  int sel_tile = -1;
-  float base = 0.f;
-  if (hit) {
-    const int L = __ffs(hit) - 1;
-    if (lane == L) {
-      float run = incl - lsum;
-      for (int t = t0; t < t1; ++t) {
-        const float m = use_resid ? ts[t].resid : ts[t].qmass;
-        if (run + m > target && m > 0.f) { sel_tile = t; base = run; break; }
-        run += m;
-      }
-      if (sel_tile < 0) {                     // rounding: take this lane's last tile with mass
-        run = incl - lsum;
-        for (int t = t0; t < t1; ++t) {
-          const float m = use_resid ? ts[t].resid : ts[t].qmass;
-          if (m > 0.f) { sel_tile = t; base = run; }
-          run += m;
+  __syncthreads();
+  const int A = s_A;
+  const int tile = s_bad ? -1 : s_sel[A];
+
+  // ---- phase 3: rescan A's selected tile, one slot per warp
+  if (tile >= 0) {
+    const int item = r * a.P + A;
+    const bool use_resid = s_resid[A] != 0;
+    const TileStats tsr = a.tiles[size_t(item) * a.ntile_stride + tile];
+    const RowStats rs = a.rows[item].s;
+    const Elem* trow = reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + A) * a.V;
+    const Elem* drow = use_resid ? reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + A) * a.V : nullptr;
+    const bool q_live = tsr.mq_c2 > neg_inf();
+    const bool p_live = use_resid && tsr.mp_c2 > neg_inf();
+    const float sq = q_live ? tile_scale(tsr.mq_c2, rs.Mq_c2, rs.Zq) : 0.f;
+    const float sp = p_live ? tile_scale(tsr.mp_c2, rs.Mp_c2, rs.Zp) : 0.f;
+    float w[(VPT + NWARP - 1) / NWARP][VW];
+#pragma unroll
+    for (int i = 0; i < (VPT + NWARP - 1) / NWARP; ++i) {
+      const int j = warp + i * NWARP;
+      if (j < VPT) {
+        S xq, xp;
+        const long idx0 = slot_index<VPT, VW>(tile, j, lane);
+        xq.load(trow, idx0, a.V);
+        if (use_resid) xp.load(drow, idx0, a.V);
+        else xp.set_neg_inf();
+        float sum = 0.f;
+        int last = -1;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          w[i][e] = draw_weight(xq, xp, e, a.c2, tsr, sq, sp, q_live, p_live, use_resid);
+          sum += w[i][e];
+          if (w[i][e] > 0.f) last = int(idx0) + e;
+        }
+        const float total = warp_sum(sum);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        if (lane == 0) {
+          s_slot[j] = total;
+          s_slot_last[j] = last;
         }
       }
     }
-    sel_tile = __shfl_sync(0xffffffffu, sel_tile, L);
-    base = __shfl_sync(0xffffffffu, base, L);
-  }
-  if (sel_tile < 0) {                          // rounding at the top: last tile with mass
-    int cand = -1;
-    for (int t = t0; t < t1; ++t)
-      if ((use_resid ? ts[t].resid : ts[t].qmass) > 0.f) cand = t;
+    __syncthreads();
+    // slot holding the target (every warp computes the same answer)
+    const float target = s_target[A];
+    float run = s_base[A];
+    int js = -1, jlast = -1, last_any = -1;
+    for (int j = 0; j < VPT; ++j) {
+      if (s_slot_last[j] >= 0) { jlast = j; last_any = s_slot_last[j]; }
+      if (js < 0 && run + s_slot[j] > target && s_slot[j] > 0.f) js = j;
+      else if (js < 0) run += s_slot[j];
+    }
+    if (js < 0) {                                  // rounding at the top: the tile's last positive weight
+      if (threadIdx.x == 0) s_tok = last_any;
+    } else if (warp == js % NWARP) {
+      const int i = js / NWARP;
+      float lsum = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-    sel_tile = cand;
-    base = 0.f;
-    // prefix before cand
-    float pre = 0.f;
-    for (int t = t0; t < t1; ++t)
-      if (t < cand) pre += use_resid ? ts[t].resid : ts[t].qmass;
-    base = warp_sum(pre);
+      for (int ii = 0; ii < (VPT + NWARP - 1) / NWARP; ++ii)
+        if (ii == i)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) lsum += w[ii][e];
+      const float incl = warp_inclusive_scan(lsum);
+      float acc = run + (incl - lsum);
+      int cand = 0x7fffffff;
+      const long idx0 = slot_index<VPT, VW>(tile, js, lane);
+#pragma unroll
+      for (int ii = 0; ii < (VPT + NWARP - 1) / NWARP; ++ii)
+        if (ii == i)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) {
+            acc += w[ii][e];
+            if (cand == 0x7fffffff && acc > target && w[ii][e] > 0.f) cand = int(idx0) + e;
+          }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+      if (lane == 0) s_tok = cand != 0x7fffffff ? cand : s_slot_last[js];
+    }
+    (void)jlast;
   }
-  int tok = -1;
-  if (sel_tile >= 0) {
-    const Elem* trow = reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + A) * a.V;
-    const Elem* drow = use_resid ? reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + A) * a.V : nullptr;
-    tok = rescan_tile<Elem, VEC, VPT>(trow, drow, a.V, sel_tile, a.c2, ts[sel_tile], rs, use_resid, base, target);
-  }
-  if (lane == 0) {
-    a.accepted[r] = A;
-    a.out_token[r] = tok;
-    if (tok < 0) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int tok = s_tok;
+    const bool bad = s_bad != 0 || tok < 0;
+    a.accepted[r] = bad ? -1 : A;
+    a.out_token[r] = bad ? -1 : tok;
+    if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
 }
 
@@ -543,10 +902,14 @@ struct Tiling {
   int vw;           // elements per slot
   int nwt;          // warp tiles per row
   int cluster;      // CTAs per row (chain_stats)
+  int stride;       // tile records per row in the workspace
+  int warps;        // warps (tiles) per CTA in chain_stats
+  int pipe;         // 1: persistent pipelined chain_stats
 };
 
 constexpr int kVptList[] = {1, 2, 4, 6, 8, 10};
 
+// 8-warp CTAs: the unaligned path and the argmax / greedy path
 bool choose_tiling(long V, specv_dtype dtype, bool vec_ok, Tiling* t) {
   const int vw = vec_ok ? (dtype == SPECV_BF16 ? 8 : 4) : 1;
   for (int pass = 0; pass < 2; ++pass) {
@@ -561,6 +924,9 @@ bool choose_tiling(long V, specv_dtype dtype, bool vec_ok, Tiling* t) {
         t->vw = vw;
         t->nwt = int(nwt);
         t->cluster = int(cl);
+        t->stride = int(cl) * kStatsWarps;
+        t->warps = kStatsWarps;
+        t->pipe = 0;
         return true;
       }
     }
@@ -568,9 +934,45 @@ bool choose_tiling(long V, specv_dtype dtype, bool vec_ok, Tiling* t) {
   return false;
 }
 
+// Persistent pipelined kernel: 16-byte rows, up to 8 CTAs per cluster of
+// kPipeWarps warps each, two CTAs per SM (measured fastest of the persistent
+// and non-persistent forms tried for the 151936-token workload).
+constexpr int kPipeWarps = 8;
+constexpr int kPipeVptBf16[] = {1, 2, 4, 6, 8, 10};
+constexpr int kPipeVptF32[] = {2, 4, 6, 8, 10};
+
+bool choose_pipe(long V, specv_dtype dtype, bool vec_ok, Tiling* t) {
+  if (!vec_ok) return false;
+  const int vw = dtype == SPECV_BF16 ? 8 : 4;
+  const int* list = dtype == SPECV_BF16 ? kPipeVptBf16 : kPipeVptF32;
+  const int nlist = dtype == SPECV_BF16 ? int(sizeof(kPipeVptBf16) / sizeof(int)) : int(sizeof(kPipeVptF32) / sizeof(int));
+  for (int i = 0; i < nlist; ++i) {
+    const long tile = 32L * list[i] * vw;
+    const long nwt = (V + tile - 1) / tile;
+    const long cl = (nwt + kPipeWarps - 1) / kPipeWarps;
+    if (cl <= 8) {
+      t->vec = 1;
+      t->vpt = list[i];
+      t->vw = vw;
+      t->nwt = int(nwt);
+      t->cluster = int(cl);
+      t->stride = int(cl) * kPipeWarps;
+      t->warps = kPipeWarps;
+      t->pipe = 1;
+      return true;
+    }
+  }
+  return false;
+}
+
+// the tiling a T > 0 call uses
+bool choose_sampling_tiling(long V, specv_dtype dtype, bool vec_ok, Tiling* t) {
+  return choose_pipe(V, dtype, vec_ok, t) || choose_tiling(V, dtype, vec_ok, t);
+}
+
 template <typename Elem, bool VEC, int VPT>
 struct ChainKernels {
-  static void* stats() { return reinterpret_cast<void*>(&chain_stats_kernel<Elem, VEC, VPT>); }
+  static void* stats() { return reinterpret_cast<void*>(&chain_stats_kernel<Elem, VEC, VPT, kStatsWarps, true>); }
   static void* finish() { return reinterpret_cast<void*>(&chain_finish_kernel<Elem, VEC, VPT>); }
   static void* argmax() { return reinterpret_cast<void*>(&argmax_tiles_kernel<Elem, VEC, VPT>); }
 };
@@ -593,7 +995,64 @@ KernelSet pick_vpt(int vpt) {
   }
 }
 
+template <typename Elem, int VPT>
+KernelSet pipe_set() {
+  return {reinterpret_cast<void*>(&chain_stats_pipe_kernel<Elem, VPT, kPipeWarps>),
+          reinterpret_cast<void*>(&chain_finish_kernel<Elem, true, VPT>), nullptr};
+}
+
+// clusters of the persistent kernel that fit at once, cached per device and kernel
+int max_active_clusters(void* fn, size_t smem, int cluster, int threads) {
+  constexpr int kSlots = 32;
+  static std::atomic<uintptr_t> keys[kSlots];
+  static std::atomic<int> vals[kSlots];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const uintptr_t key = (reinterpret_cast<uintptr_t>(fn) ^ (uintptr_t(dev) << 48) ^ (uintptr_t(cluster) << 56)) | 1;
+  for (int i = 0; i < kSlots; ++i)
+    if (keys[i].load(std::memory_order_acquire) == key) return vals[i].load(std::memory_order_relaxed);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(cluster) * 64);
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = unsigned(cluster);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+  for (int i = 0; i < kSlots; ++i) {
+    uintptr_t expected = 0;
+    if (keys[i].load(std::memory_order_relaxed) == 0 && keys[i].compare_exchange_strong(expected, key)) {
+      vals[i].store(n, std::memory_order_relaxed);
+      break;
+    }
+  }
+  return n;
+}
+
 KernelSet kernels_for(specv_dtype dtype, const Tiling& t) {
+  if (t.pipe) {
+    if (dtype == SPECV_BF16)
+      switch (t.vpt) {
+        case 1: return pipe_set<uint16_t, 1>();
+        case 2: return pipe_set<uint16_t, 2>();
+        case 4: return pipe_set<uint16_t, 4>();
+        case 6: return pipe_set<uint16_t, 6>();
+        case 8: return pipe_set<uint16_t, 8>();
+        default: return pipe_set<uint16_t, 10>();
+      }
+    switch (t.vpt) {
+      case 2: return pipe_set<float, 2>();
+      case 4: return pipe_set<float, 4>();
+      case 6: return pipe_set<float, 6>();
+      case 8: return pipe_set<float, 8>();
+      default: return pipe_set<float, 10>();
+    }
+  }
   if (dtype == SPECV_BF16) return t.vec ? pick_vpt<uint16_t, true>(t.vpt) : pick_vpt<uint16_t, false>(t.vpt);
   return t.vec ? pick_vpt<float, true>(t.vpt) : pick_vpt<float, false>(t.vpt);
 }
@@ -607,7 +1066,7 @@ struct ChainLayout {
 
 ChainLayout chain_layout(int R, int gamma, const Tiling& t) {
   ChainLayout L;
-  L.ntile_stride = t.cluster * kStatsWarps;
+  L.ntile_stride = t.stride;
   const size_t items = size_t(R) * (gamma + 1);
   size_t off = kHeaderBytes;
   L.rows_off = off;
@@ -627,11 +1086,38 @@ bool rows_vector_ok(const void* p, long V, specv_dtype dtype) {
   return p == nullptr || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && V % vw == 0);
 }
 
-specv_status launch_stats(const KernelSet& ks, const Tiling& t, const StatsArgs& sa, int items, cudaStream_t st) {
+specv_status launch_stats(const KernelSet& ks, const Tiling& t, const StatsArgs& sa, int items, cudaStream_t st,
+                          specv_dtype dtype) {
   if (items == 0) return SPECV_OK;
+  if (t.pipe) {
+    const size_t smem = size_t(2) * t.vpt * t.warps * 32 * sizeof(uint4);
+    if (cudaFuncSetAttribute(ks.stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+      return SPECV_ERR_CUDA;
+    const int maxcl = max_active_clusters(ks.stats, smem, t.cluster, t.warps * 32);
+    if (maxcl < 1) return SPECV_ERR_UNSUPPORTED;
+    PipeArgs pa;
+    pa.s = sa;
+    pa.items = items;
+    pa.ncl = items < maxcl ? items : maxcl;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(pa.ncl) * unsigned(t.cluster));
+    cfg.blockDim = dim3(unsigned(t.warps) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = unsigned(t.cluster);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    void* args[] = {&pa};
+    if (cudaLaunchKernelExC(&cfg, ks.stats, args) != cudaSuccess) return SPECV_ERR_CUDA;
+    return SPECV_OK;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(items) * unsigned(t.cluster));
-  cfg.blockDim = dim3(kStatsWarps * 32);
+  cfg.blockDim = dim3(unsigned(t.warps) * 32);
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -644,6 +1130,11 @@ specv_status launch_stats(const KernelSet& ks, const Tiling& t, const StatsArgs&
     if (cudaFuncSetAttribute(ks.stats, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return SPECV_ERR_CUDA;
   }
+  const size_t smem = t.vec ? size_t(t.warps) * t.vpt * (t.vw / 4) * 32 * sizeof(float4) : 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(ks.stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  cfg.dynamicSmemBytes = smem;
   void* args[] = {const_cast<StatsArgs*>(&sa)};
   if (cudaLaunchKernelExC(&cfg, ks.stats, args) != cudaSuccess) return SPECV_ERR_CUDA;
   return SPECV_OK;
@@ -676,11 +1167,12 @@ static specv_status chain_sampling(const void* target, const void* draft, specv_
   sa.ntile_stride = L.ntile_stride;
   sa.with_bonus = sample ? 1 : 0;
   sa.c2 = kLog2e / T;
-  specv_status s = launch_stats(ks, t, sa, R * P, st);
+  specv_status s = launch_stats(ks, t, sa, R * P, st, dtype);
   if (s != SPECV_OK) return s;
   FinishArgs fa;
   fa.target = target;
   fa.draft = draft;
+  fa.tokens = tokens;
   fa.lengths = lengths;
   fa.uniforms = uniforms;
   fa.rows = sa.rows;
@@ -699,7 +1191,18 @@ static specv_status chain_sampling(const void* target, const void* draft, specv_
   fa.c2 = sa.c2;
   fa.sample = sample ? 1 : 0;
   void* fargs[] = {&fa};
-  if (cudaLaunchKernel(ks.finish, dim3(R), dim3(kFinishThreads), fargs, 0, st) != cudaSuccess) return SPECV_ERR_CUDA;
+  // programmatic dependent launch: the finish grid is scheduled while the stats
+  // grid drains and waits (griddepcontrol.wait) for its results
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(R));
+  cfg.blockDim = dim3(kFinishThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, ks.finish, fargs) != cudaSuccess) return SPECV_ERR_CUDA;
   return SPECV_OK;
 }
 
@@ -790,6 +1293,9 @@ specv_status launch_argmax_rows(const ArgmaxPlan& p, specv_dtype dtype, const vo
   t.vw = 0;
   t.nwt = p.nwt;
   t.cluster = p.stride / kStatsWarps;
+  t.stride = p.stride;
+  t.warps = kStatsWarps;
+  t.pipe = 0;
   const KernelSet ks = kernels_for(dtype, t);
   return launch_argmax(ks, t, logits, lengths, ws, out, R, P, Pout, lim_off, gamma, V, p.stride, clear_error, st);
 }
@@ -803,9 +1309,13 @@ extern "C" size_t specv_verify_chain_workspace_size(int R, int gamma, int V, spe
   // enough for whichever tiling a call may pick (aligned or unaligned rows)
   size_t need = 0;
   for (int vec = 0; vec < 2; ++vec) {
-    Tiling t;
     if (vec && V % (dtype == SPECV_BF16 ? 8 : 4) != 0) continue;
+    Tiling t;
     if (choose_tiling(V, dtype, vec != 0, &t)) {
+      const size_t n = chain_layout(R, gamma, t).total;
+      if (n > need) need = n;
+    }
+    if (choose_pipe(V, dtype, vec != 0, &t)) {
       const size_t n = chain_layout(R, gamma, t).total;
       if (n > need) need = n;
     }
@@ -839,7 +1349,8 @@ extern "C" specv_status specv_verify_chain(const void* target_logits, const void
     return SPECV_ERR_INVALID_ARG;
   const bool vec_ok = rows_vector_ok(target_logits, V, dtype) && rows_vector_ok(draft_logits, V, dtype);
   Tiling t;
-  if (!choose_tiling(V, dtype, vec_ok, &t)) return SPECV_ERR_UNSUPPORTED;
+  if (temperature > 0.f ? !choose_sampling_tiling(V, dtype, vec_ok, &t) : !choose_tiling(V, dtype, vec_ok, &t))
+    return SPECV_ERR_UNSUPPORTED;
   if (workspace_bytes < chain_layout(R, gamma, t).total) return SPECV_ERR_INVALID_ARG;
   specv_status s = check_device();
   if (s != SPECV_OK) return s;
@@ -869,7 +1380,8 @@ extern "C" specv_status specv_tv_accept(const void* target_logits, const void* d
     return SPECV_ERR_INVALID_ARG;
   const bool vec_ok = rows_vector_ok(target_logits, V, dtype) && rows_vector_ok(draft_logits, V, dtype);
   Tiling t;
-  if (!choose_tiling(V, dtype, vec_ok, &t)) return SPECV_ERR_UNSUPPORTED;
+  if (temperature > 0.f ? !choose_sampling_tiling(V, dtype, vec_ok, &t) : !choose_tiling(V, dtype, vec_ok, &t))
+    return SPECV_ERR_UNSUPPORTED;
   if (workspace_bytes < chain_layout(R, gamma, t).total) return SPECV_ERR_INVALID_ARG;
   specv_status s = check_device();
   if (s != SPECV_OK) return s;

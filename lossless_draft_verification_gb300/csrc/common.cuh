@@ -115,6 +115,75 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine) primitives, inline PTX
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// `max_iter` polls (each poll itself blocks for a hardware-defined interval).
+// Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_parity(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < max_iter; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// per-thread 16-byte asynchronous global -> shared copies (Ampere-style cp.async)
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+
+// programmatic dependent launch
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// packed float32 pairs (sm_100+): two IEEE round-to-nearest operations per
+// instruction, through the compiler's builtins so that it allocates the pairs
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // register tiles of logits
 //
 // Elem = uint16_t (bf16 bits) or float.  VEC selects 16-byte vectors (rows
@@ -144,6 +213,15 @@ struct Slot {
     }
   }
 
+  __device__ __forceinline__ void set_neg_inf() {
+    if constexpr (VEC) {
+      const uint32_t ninf = sizeof(Elem) == 2 ? (kBf16NegInf | (kBf16NegInf << 16)) : kF32NegInfBits;
+      w[0] = w[1] = w[2] = w[3] = ninf;
+    } else {
+      w[0] = kF32NegInfBits;
+    }
+  }
+
   // load elements [idx, idx + VW) of `row` (length V); out-of-row lanes read -inf
   __device__ __forceinline__ void load(const Elem* row, long idx, long V) {
     if constexpr (VEC) {
@@ -162,6 +240,19 @@ struct Slot {
       } else {
         w[0] = kF32NegInfBits;
       }
+    }
+  }
+
+  // element e, unpacked by an opaque instruction: the compiler cannot reuse a
+  // conversion from an earlier pass, which would keep the unpacked floats live
+  __device__ __forceinline__ float get_fresh(int e) const {
+    if constexpr (VEC && sizeof(Elem) == 2) {
+      uint32_t r;
+      if (e & 1) asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(r) : "r"(w[e >> 1]));
+      else asm volatile("shl.b32 %0, %1, 16;" : "=r"(r) : "r"(w[e >> 1]));
+      return __uint_as_float(r);
+    } else {
+      return get(e);
     }
   }
 
