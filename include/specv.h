@@ -49,7 +49,8 @@
  *  - Logits may be float32 or bfloat16 (SPECV_F32 / SPECV_BF16).  All
  *    arithmetic is float32; argmax compares the stored values exactly and
  *    resolves ties to the lowest token id.  Logits must be finite.
- *  - Thread-safe: no global state other than a per-device capability cache.
+ *  - Thread-safe: no global state other than a per-device capability cache
+ *    and the built-in scratch of specv_verify_chain_noalloc.
  */
 #ifndef SPECV_H_
 #define SPECV_H_
@@ -73,6 +74,7 @@ extern "C" {
 #define SPECV_MAX_TREE_DEPTH 64
 #define SPECV_MAX_SCHED_ENTRIES 8192 /* R * gamma for specv_schedule              */
 #define SPECV_MAX_MARKOV_RANK 1024
+#define SPECV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* specv_verify_chain_noalloc */
 
 typedef enum {
   SPECV_OK = 0,
@@ -80,7 +82,9 @@ typedef enum {
   SPECV_ERR_UNSUPPORTED = 2,   /* valid request the build cannot serve (device, size)   */
   SPECV_ERR_CUDA = 3,          /* a CUDA call or launch failed                          */
   SPECV_ERR_DEVICE_DATA = 4,   /* device-detected bad data (outputs of that request = -1) */
-  SPECV_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up                    */
+  SPECV_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up                    */
+  SPECV_ERR_SCRATCH_LIMIT = 6  /* shape needs more than specv_verify_chain_noalloc's
+                                  built-in scratch (SPECV_NOALLOC_SCRATCH_BYTES)        */
 } specv_status;
 
 typedef enum { SPECV_F32 = 0, SPECV_BF16 = 1 } specv_dtype;
@@ -136,6 +140,38 @@ SPECV_API specv_status specv_verify_chain(const void* target_logits, const void*
                                 int R, int gamma, int V, float temperature,
                                 int32_t* accepted_len, int32_t* out_token, float* c_star,
                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * specv_verify_chain_noalloc -- specv_verify_chain without a caller workspace.
+ *
+ * The pages have no counterpart: this is a library convenience.  It computes
+ * exactly what specv_verify_chain computes, with the same kernels and
+ * arguments minus (workspace, workspace_bytes).  The scratch is a static
+ * device buffer of SPECV_NOALLOC_SCRATCH_BYTES (16 MiB) per device, built into
+ * the library, so the call allocates and frees nothing.  It serves callers
+ * that cannot hand over device memory: code running inside an allocator or
+ * memory-pool callback, servers that forbid device allocation once their
+ * weights and KV cache are placed, C hosts without a device allocator.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ *   the buffer's device address with cudaGetSymbolAddress, which may load the
+ *   library's device module; make that first call outside any stream capture.
+ * Concurrency: all calls on one device share the one buffer.  Calls whose
+ *   execution may overlap (different streams, or host threads enqueueing
+ *   without ordering) race on it and give undefined results; serialise them
+ *   on one stream.
+ * Device-detected bad data still gives -1 outputs for the request; the error
+ *   word itself stays inside the built-in buffer and is not readable.
+ * Errors: as specv_verify_chain; SPECV_ERR_INVALID_ARG also when
+ *   specv_verify_chain_workspace_size(R, gamma, V, dtype) is 0, and
+ *   SPECV_ERR_SCRATCH_LIMIT when it exceeds SPECV_NOALLOC_SCRATCH_BYTES
+ *   (e.g. R = 1024, gamma = 7, V = 151936 bf16 needs about 15.6 MiB and fits;
+ *   R = 2048 does not).  Both are decided on the host before any CUDA call.
+ */
+SPECV_API specv_status specv_verify_chain_noalloc(const void* target_logits, const void* draft_logits,
+                                       specv_dtype dtype, const int32_t* draft_tokens, const int32_t* lengths,
+                                       const float* uniforms, int R, int gamma, int V, float temperature,
+                                       int32_t* accepted_len, int32_t* out_token, float* c_star, void* stream);
 
 /* ------------------------------------------------------------------ c* */
 

@@ -22,15 +22,16 @@ import os
 
 __all__ = [
     "load", "SpecvError", "SPECV_OK", "SPECV_ERR_INVALID_ARG", "SPECV_ERR_UNSUPPORTED", "SPECV_ERR_CUDA",
-    "SPECV_ERR_DEVICE_DATA", "SPECV_ERR_TIMEOUT", "SPECV_F32", "SPECV_BF16", "EXPORTED",
-    "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_tv_accept_workspace_size", "specv_tv_accept",
+    "SPECV_ERR_DEVICE_DATA", "SPECV_ERR_TIMEOUT", "SPECV_ERR_SCRATCH_LIMIT", "SPECV_F32", "SPECV_BF16", "EXPORTED",
+    "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_verify_chain_noalloc", "specv_tv_accept_workspace_size", "specv_tv_accept",
     "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
     "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_read_device_error",
     "specv_status_string", "specv_abi_version",
     "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "read_device_error",
 ]
 
-SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_DEVICE_DATA, SPECV_ERR_TIMEOUT = range(6)
+(SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_DEVICE_DATA, SPECV_ERR_TIMEOUT,
+ SPECV_ERR_SCRATCH_LIMIT) = range(7)
 SPECV_F32, SPECV_BF16 = 0, 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libspecv.so")
@@ -42,6 +43,8 @@ EXPORTED = {
     "specv_verify_chain_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "specv_verify_chain": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
                                     _vp, _c_size, _vp]),
+    "specv_verify_chain_noalloc": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp,
+                                            _vp, _vp]),
     "specv_tv_accept_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "specv_tv_accept": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _c_size, _vp]),
     "specv_verify_tree_greedy_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
@@ -101,6 +104,12 @@ def specv_verify_chain(target_logits, draft_logits, dtype, draft_tokens, lengths
                        accepted_len, out_token, c_star, workspace, workspace_bytes, stream):
     return _call("specv_verify_chain", target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms, R, gamma,
                  V, temperature, accepted_len, out_token, c_star, workspace, workspace_bytes, stream)
+
+
+def specv_verify_chain_noalloc(target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms, R, gamma, V,
+                               temperature, accepted_len, out_token, c_star, stream):
+    return _call("specv_verify_chain_noalloc", target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms, R,
+                 gamma, V, temperature, accepted_len, out_token, c_star, stream)
 
 
 def specv_tv_accept_workspace_size(R, gamma, V, dtype):

@@ -41,6 +41,7 @@ extern "C" const char* specv_status_string(specv_status status) {
     case SPECV_ERR_CUDA: return "CUDA error";
     case SPECV_ERR_DEVICE_DATA: return "device-detected invalid data";
     case SPECV_ERR_TIMEOUT: return "bounded device wait expired";
+    case SPECV_ERR_SCRATCH_LIMIT: return "shape exceeds the built-in scratch of the allocation-free call";
   }
   return "unknown status";
 }
