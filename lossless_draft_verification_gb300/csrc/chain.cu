@@ -354,6 +354,17 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     }
   };
 
+  // Slots past the end of the row are never copied into: fill them with -inf
+  // once, so that every item reads its slots without a per-slot select.
+  {
+    const uint32_t ninf = sizeof(Elem) == 2 ? (kBf16NegInf | (kBf16NegInf << 16)) : kF32NegInfBits;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+      if (!active || slot_index<VPT, VW>(tile, j, lane) >= V) {
+        *stage(0, j) = make_uint4(ninf, ninf, ninf, ninf);
+        *stage(1, j) = make_uint4(ninf, ninf, ninf, ninf);
+      }
+  }
   prefetch(cid);
   cp_async_commit();
   int processed = 0;
@@ -363,33 +374,39 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     int r, k;
     const int kind = decode(item, r, k);
     cp_async_wait_all();                         // this thread's copies of `item` have landed
+    // (the draft half of the stage is stale for a bonus row: its p results are dropped)
     S tq[VPT], tp[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const bool in = kind != 0 && active && slot_index<VPT, VW>(tile, j, lane) < V;
-      if (in) {
-        const uint4 v = *stage(0, j);
-        tq[j].w[0] = v.x; tq[j].w[1] = v.y; tq[j].w[2] = v.z; tq[j].w[3] = v.w;
-      } else {
-        tq[j].set_neg_inf();
-      }
-      if (in && kind == 1) {
-        const uint4 v = *stage(1, j);
-        tp[j].w[0] = v.x; tp[j].w[1] = v.y; tp[j].w[2] = v.z; tp[j].w[3] = v.w;
-      } else {
-        tp[j].set_neg_inf();
-      }
+      const uint4 v = *stage(0, j);
+      tq[j].w[0] = v.x; tq[j].w[1] = v.y; tq[j].w[2] = v.z; tq[j].w[3] = v.w;
+      const uint4 u = *stage(1, j);
+      tp[j].w[0] = u.x; tp[j].w[1] = u.y; tp[j].w[2] = u.z; tp[j].w[3] = u.w;
     }
     // tile maxima: consumes every staged value, so the slots are free to refill
     float mq = neg_inf(), mp = neg_inf();
+    if constexpr (sizeof(Elem) == 2) {
+      uint32_t aq = tq[0].w[0], ap = tp[0].w[0];
 #pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      mq = fmaxf(mq, tq[j].vmax());
-      mp = fmaxf(mp, tp[j].vmax());
+      for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int i = (j == 0 ? 1 : 0); i < 4; ++i) {
+          asm("max.bf16x2 %0, %1, %2;" : "=r"(aq) : "r"(aq), "r"(tq[j].w[i]));
+          asm("max.bf16x2 %0, %1, %2;" : "=r"(ap) : "r"(ap), "r"(tp[j].w[i]));
+        }
+      mq = fmaxf(__uint_as_float(aq << 16), __uint_as_float(aq & 0xFFFF0000u));
+      mp = fmaxf(__uint_as_float(ap << 16), __uint_as_float(ap & 0xFFFF0000u));
+    } else {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        mq = fmaxf(mq, tq[j].vmax());
+        mp = fmaxf(mp, tp[j].vmax());
+      }
     }
     prefetch(cid + (n + 1) * pa.ncl);
     cp_async_commit();
     if (kind == 0) continue;
+    if (kind == 2) mp = neg_inf();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
@@ -414,15 +431,14 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         }
       return (za.x + za.y) + (zb.x + zb.y);
     };
-    float zq = tile_sum(tq, mq_c2);
-    float zp = tile_sum(tp, mp_c2);
+    float zq = 0.f, zp = 0.f;
+    if (q_live) zq = tile_sum(tq, mq_c2);
+    if (p_live) zp = tile_sum(tp, mp_c2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       zq += __shfl_xor_sync(0xffffffffu, zq, o);
       zp += __shfl_xor_sync(0xffffffffu, zp, o);
     }
-    if (!q_live) zq = 0.f;
-    if (!p_live) zp = 0.f;
 
     // ---- CTA partial, then the cluster-wide row statistics
     const int pb = processed & 1;
@@ -478,12 +494,17 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
       lp = p_live ? lp - mp_c2 : neg_inf();
       float2 ma = make_float2(0.f, 0.f), mb = ma;
 #pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        tq[j].launder();
+        tp[j].launder();
+      }
+#pragma unroll
       for (int j = 0; j < VPT; ++j)
 #pragma unroll
         for (int e = 0; e < VW; e += 2) {
-          const float2 t = fma2(make_float2(tq[j].get_fresh(e), tq[j].get_fresh(e + 1)), make_float2(c2, c2),
+          const float2 t = fma2(make_float2(tq[j].get(e), tq[j].get(e + 1)), make_float2(c2, c2),
                                 make_float2(lq, lq));
-          const float2 u = fma2(make_float2(tp[j].get_fresh(e), tp[j].get_fresh(e + 1)), make_float2(c2, c2),
+          const float2 u = fma2(make_float2(tp[j].get(e), tp[j].get(e + 1)), make_float2(c2, c2),
                                 make_float2(lp, lp));
           const float2 mn = make_float2(ex2(fminf(t.x, u.x)), ex2(fminf(t.y, u.y)));
           if ((e >> 1) & 1) mb = add2(mb, mn); else ma = add2(ma, mn);

@@ -256,6 +256,14 @@ struct Slot {
     }
   }
 
+  // make the words opaque to the compiler (values unchanged), so that a later
+  // pass re-derives its floats from them instead of keeping an earlier pass's
+  // unpacked floats alive
+  __device__ __forceinline__ void launder() {
+#pragma unroll
+    for (int i = 0; i < Lanes<Elem, VEC>::REGS; ++i) asm volatile("" : "+r"(w[i]));
+  }
+
   // maximum element (exact)
   __device__ __forceinline__ float vmax() const {
     if constexpr (VEC && sizeof(Elem) == 2) {
