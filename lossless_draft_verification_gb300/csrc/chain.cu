@@ -293,9 +293,10 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_kernel(StatsArgs a) {
 // next item into a private area of shared memory with 16-byte cp.async copies
 // while the current item is processed from registers (no block-wide sync is
 // needed for the staging: a thread only reads what it copied).  Pass 2
-// recomputes the exponentials from the registers.  Tile partials are
-// exchanged through distributed shared memory, double-buffered by the parity of
-// the processed-item count so that one cluster barrier per item suffices.
+// recomputes the exponentials from the registers.  After pass 1 every warp
+// stores its tile partial into each CTA of the cluster (distributed shared
+// memory, double-buffered by the parity of the processed-item count), so one
+// cluster barrier per item makes all partials local to every warp.
 struct PipeArgs {
   StatsArgs s;
   int items;        // R * P
@@ -306,10 +307,11 @@ template <typename Elem, int VPT, int NW>
 __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs pa) {
   using S = Slot<Elem, true>;
   constexpr int VW = S::VW;
+  constexpr int kMaxParts = 8 * NW;             // cluster of at most 8 CTAs
+  static_assert(kMaxParts <= 64, "two partials per lane");
   const StatsArgs& a = pa.s;
   extern __shared__ uint4 s_stage[];            // [2 rows][VPT][threads]
-  __shared__ float4 s_warp[2][NW];
-  __shared__ float4 s_cta[2];
+  __shared__ float4 s_part[2][kMaxParts];       // every warp's partial of the cluster
 
   const uint32_t C = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
@@ -321,9 +323,22 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
   const float c2 = a.c2;
   if (cid == 0 && rank == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
-  auto decode = [&](int item, int& r, int& k) -> int {   // 0 skip, 1 row pair, 2 bonus row
-    r = item / a.P;
-    k = item - r * a.P;
+  // this thread's slots: elements [base + j*32*VW, +VW) for j < jmax are in the row
+  const long base = (long(tile) * 32 * VPT + lane) * VW;
+  int jmax = 0;
+  if (active && base < V) {
+    const long n = (V - base + 32 * VW - 1) / (32 * VW);
+    jmax = n < VPT ? int(n) : VPT;
+  }
+
+  // items of this cluster: item = cid + n * ncl, decoded incrementally into (r, k)
+  const int dr = pa.ncl / a.P, dk = pa.ncl - (pa.ncl / a.P) * a.P;
+  auto advance = [&](int& r, int& k) {
+    r += dr;
+    k += dk;
+    if (k >= a.P) { k -= a.P; ++r; }
+  };
+  auto kind_of = [&](int r, int k) -> int {      // 0 skip, 1 row pair, 2 bonus row
     int ell = a.gamma;
     if (a.lengths) {
       ell = __ldg(a.lengths + r);
@@ -333,25 +348,22 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     return (a.with_bonus && k == ell) ? 2 : 0;
   };
   auto stage = [&](int row, int j) -> uint4* { return s_stage + (row * VPT + j) * (NW * 32) + threadIdx.x; };
-  auto prefetch = [&](int item) {
-    if (item >= pa.items || !active) return;
-    int r, k;
-    const int kind = decode(item, r, k);
+  auto copy_row = [&](int row, const Elem* src) {
+    if (jmax == VPT) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) cp_async16(stage(row, j), src + base + j * 32 * VW);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < jmax) cp_async16(stage(row, j), src + base + j * 32 * VW);
+    }
+  };
+  auto prefetch = [&](int item, int r, int k) {
+    if (item >= pa.items || jmax == 0) return;
+    const int kind = kind_of(r, k);
     if (kind == 0) return;
-    const Elem* trow = reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * size_t(V);
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      const long idx = slot_index<VPT, VW>(tile, j, lane);
-      if (idx < V) cp_async16(stage(0, j), trow + idx);
-    }
-    if (kind == 1) {
-      const Elem* drow = reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + k) * size_t(V);
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const long idx = slot_index<VPT, VW>(tile, j, lane);
-        if (idx < V) cp_async16(stage(1, j), drow + idx);
-      }
-    }
+    copy_row(0, reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * size_t(V));
+    if (kind == 1) copy_row(1, reinterpret_cast<const Elem*>(a.draft) + (size_t(r) * a.Pd + k) * size_t(V));
   };
 
   // Slots past the end of the row are never copied into: fill them with -inf
@@ -360,19 +372,19 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     const uint32_t ninf = sizeof(Elem) == 2 ? (kBf16NegInf | (kBf16NegInf << 16)) : kF32NegInfBits;
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
-      if (!active || slot_index<VPT, VW>(tile, j, lane) >= V) {
+      if (j >= jmax) {
         *stage(0, j) = make_uint4(ninf, ninf, ninf, ninf);
         *stage(1, j) = make_uint4(ninf, ninf, ninf, ninf);
       }
   }
-  prefetch(cid);
+  int r = cid / a.P, k = cid - (cid / a.P) * a.P;        // current item
+  int rn = r, kn = k;                                    // next item
+  advance(rn, kn);
+  prefetch(cid, r, k);
   cp_async_commit();
   int processed = 0;
-  for (int n = 0;; ++n) {
-    const int item = cid + n * pa.ncl;
-    if (item >= pa.items) break;
-    int r, k;
-    const int kind = decode(item, r, k);
+  for (int item = cid; item < pa.items; item += pa.ncl, r = rn, k = kn, advance(rn, kn)) {
+    const int kind = kind_of(r, k);
     cp_async_wait_all();                         // this thread's copies of `item` have landed
     // (the draft half of the stage is stale for a bonus row: its p results are dropped)
     S tq[VPT], tp[VPT];
@@ -403,7 +415,7 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         mp = fmaxf(mp, tp[j].vmax());
       }
     }
-    prefetch(cid + (n + 1) * pa.ncl);
+    prefetch(item + pa.ncl, rn, kn);
     cp_async_commit();
     if (kind == 0) continue;
     if (kind == 2) mp = neg_inf();
@@ -440,41 +452,27 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
       zp += __shfl_xor_sync(0xffffffffu, zp, o);
     }
 
-    // ---- CTA partial, then the cluster-wide row statistics
+    // ---- every warp's partial into every CTA, one cluster barrier, then the
+    // row statistics from the C * NW local partials
     const int pb = processed & 1;
-    if (lane == 0) s_warp[pb][warp] = make_float4(q_live ? mq_c2 : neg_inf(), zq, p_live ? mp_c2 : neg_inf(), zp);
-    __syncthreads();
-    if (warp == 0) {
-      const float4 w = lane < NW ? s_warp[pb][lane] : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
-      float Mq = w.x, Mp = w.z;
-#pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) {
-        Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, o));
-        Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, o));
-      }
-      float Zq = w.y > 0.f ? w.y * ex2(w.x - Mq) : 0.f;
-      float Zp = w.w > 0.f ? w.w * ex2(w.z - Mp) : 0.f;
-#pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) {
-        Zq += __shfl_xor_sync(0xffffffffu, Zq, o);
-        Zp += __shfl_xor_sync(0xffffffffu, Zp, o);
-      }
-      if (lane == 0) s_cta[pb] = make_float4(Mq, Zq, Mp, Zp);
-      cluster_arrive_release();
-    } else {
-      cluster_arrive_relaxed();
+    {
+      const float4 part = make_float4(q_live ? mq_c2 : neg_inf(), zq, p_live ? mp_c2 : neg_inf(), zp);
+      if (lane < int(C)) st_shared_cluster_f4(cluster_map_shared(&s_part[pb][rank * NW + warp], uint32_t(lane)), part);
     }
+    cluster_arrive_release();
     cluster_wait_acquire();
-    const float4 cc = lane < int(C) ? ld_shared_cluster_f4(cluster_map_shared(&s_cta[pb], uint32_t(lane)))
-                                    : make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
-    float Mq = cc.x, Mp = cc.z;
+    const int nparts = int(C) * NW;
+    const float4 none = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+    const float4 w0 = lane < nparts ? s_part[pb][lane] : none;
+    const float4 w1 = lane + 32 < nparts ? s_part[pb][lane + 32] : none;
+    float Mq = fmaxf(w0.x, w1.x), Mp = fmaxf(w0.z, w1.z);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {             // every lane needs the row statistics
       Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, o));
       Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, o));
     }
-    float Zq = cc.y > 0.f ? cc.y * ex2(cc.x - Mq) : 0.f;
-    float Zp = cc.w > 0.f ? cc.w * ex2(cc.z - Mp) : 0.f;
+    float Zq = (w0.y > 0.f ? w0.y * ex2(w0.x - Mq) : 0.f) + (w1.y > 0.f ? w1.y * ex2(w1.x - Mq) : 0.f);
+    float Zp = (w0.w > 0.f ? w0.w * ex2(w0.z - Mp) : 0.f) + (w1.w > 0.f ? w1.w * ex2(w1.z - Mp) : 0.f);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Zq += __shfl_xor_sync(0xffffffffu, Zq, o);
@@ -529,9 +527,9 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     }
     ++processed;
   }
+  // Every store into this CTA's partials precedes the barrier of the last
+  // item, and all reads are local: no exit barrier is needed.
   cp_async_wait_all();
-  cluster_arrive_release();            // no CTA leaves while another may still read its partials
-  cluster_wait_acquire();
   pdl_launch_dependents();
 }
 

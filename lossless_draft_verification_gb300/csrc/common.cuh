@@ -107,6 +107,11 @@ __device__ __forceinline__ uint32_t cluster_map_shared(const void* p, uint32_t r
   return remote;
 }
 
+__device__ __forceinline__ void st_shared_cluster_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
