@@ -11,6 +11,15 @@ fraction of the measured copy bandwidth.
 `--impl reference` times the CPU oracle (the reference arm of this repo) on the
 same workload, one bounded sample of requests per step.
 
+`--workload` selects another row of the hot path for its own JSON line (the
+default is the headline chain workload above):
+  greedy    T = 0 chain verification, R=64, gamma=7, V=151936 (target rows only)
+  tv        standalone c* (specv_tv_accept), R=64, gamma=7, V=151936, T = 1
+  tree      greedy tree verification, R=16 trees of 60 nodes + root, V=151936
+  markov    DSpark Markov head, R=512, gamma=7, V=129280, rank 256, T = 1,
+            float32 logits written
+  schedule  greedy scheduler, R=512, gamma=7, SPS table of 4096 entries
+
 Multi-GPU (torchrun): every rank verifies its own batch (requests are
 independent; no collective on the data path); value = all ranks' positions /
 max-over-ranks time.
@@ -309,6 +318,154 @@ def run_ours(args):
     return 0
 
 
+def _timed(call, flush, steps, warmup, stream):
+    import torch
+    for _ in range(max(3, warmup)):
+        if flush is not None:
+            flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s_, e_ in ev:
+        if flush is not None:
+            flush.zero_()
+        s_.record(stream)
+        call()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    return statistics.fmean(s_.elapsed_time(e_) for s_, e_ in ev), clocks
+
+
+def run_workload(args):
+    """One JSON line for a non-headline row of the path (device-resident inputs)."""
+    import numpy as np
+    import torch
+
+    import lossless_draft_verification_gb300 as specv
+    from lossless_draft_verification_gb300 import build as _build
+    import synth
+
+    _build.build()
+    specv.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    td = lambda a, kind=None: torch.from_numpy(np.ascontiguousarray(a if kind is None else a.astype(kind))).to(dev)
+    bf = lambda lg: td(lg.raw.view(np.int16)).view(torch.bfloat16)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    peak, peak_kind = _peak_hbm()
+    w = args.workload
+
+    def check(st, name):
+        if st != 0:
+            raise specv.SpecvError(st, name)
+
+    if w in ("greedy", "tv"):
+        case = synth.chain_batched(seed=3, R=R, temperature=1.0)
+        target, draft = bf(case.target), bf(case.draft)
+        if w == "greedy":
+            x = td(case.tokens, np.int32)
+            acc = torch.empty(R, dtype=torch.int32, device=dev)
+            tok = torch.empty(R, dtype=torch.int32, device=dev)
+            nb = specv.specv_verify_chain_workspace_size(R, GAMMA, V, specv.SPECV_BF16)
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            call = lambda: check(specv.specv_verify_chain(target.data_ptr(), None, specv.SPECV_BF16, x.data_ptr(), None,
+                                                          None, R, GAMMA, V, 0.0, acc.data_ptr(), tok.data_ptr(), None,
+                                                          ws.data_ptr(), nb, sp), "specv_verify_chain")
+            algo = R * (GAMMA + 1) * V * 2
+            units, unit, metric = R * GAMMA, "positions/s", "greedy chain verification: verified draft positions/sec"
+            desc, launches = "greedy chain verify: R=64, gamma=7, V=151936 bf16, T=0 (target rows only)", 2
+            kernel = "argmax tiles + greedy finish (whole call)"
+        else:
+            cst = torch.empty(R, GAMMA, dtype=torch.float32, device=dev)
+            nb = specv.specv_tv_accept_workspace_size(R, GAMMA, V, specv.SPECV_BF16)
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            call = lambda: check(specv.specv_tv_accept(target.data_ptr(), draft.data_ptr(), specv.SPECV_BF16, R, GAMMA,
+                                                       GAMMA + 1, V, 1.0, cst.data_ptr(), ws.data_ptr(), nb, sp),
+                                 "specv_tv_accept")
+            algo = 2 * R * GAMMA * V * 2
+            units, unit, metric = R * GAMMA, "positions/s", "analytic acceptance c*: (request, position) pairs/sec"
+            desc, launches = "tv_accept: R=64, gamma=7, V=151936 bf16, T=1", 2
+            kernel = "chain_stats + c* finish (whole call)"
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
+    elif w == "tree":
+        case = synth.tree_greedy(seed=4)
+        Rt, N1, Vt = case.target.raw.shape
+        target = bf(case.target)
+        par, tks = td(case.parents, np.int32), td(case.tokens, np.int32)
+        plen = torch.empty(Rt, dtype=torch.int32, device=dev)
+        nodes = torch.empty(Rt, case.max_depth, dtype=torch.int32, device=dev)
+        tok = torch.empty(Rt, dtype=torch.int32, device=dev)
+        nb = specv.specv_verify_tree_greedy_workspace_size(Rt, N1 - 1, Vt, specv.SPECV_BF16)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        call = lambda: check(specv.specv_verify_tree_greedy(target.data_ptr(), specv.SPECV_BF16, par.data_ptr(),
+                                                            tks.data_ptr(), Rt, N1 - 1, Vt, case.max_depth,
+                                                            plen.data_ptr(), nodes.data_ptr(), tok.data_ptr(),
+                                                            ws.data_ptr(), nb, sp), "specv_verify_tree_greedy")
+        algo = Rt * N1 * Vt * 2
+        units, unit, metric = Rt * (N1 - 1), "nodes/s", "greedy tree verification: candidate nodes verified/sec"
+        desc, launches, kernel = "greedy tree: R=16 trees, 60 nodes + root, depth <= 8, V=151936 bf16", 1, "tree_walk"
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
+    elif w == "markov":
+        Rm, Gm, Vm, rank = 512, 7, 129280, 256
+        m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
+        U, W1, W2 = bf(m.U), bf(m.W1), bf(m.W2)
+        anchor, u = td(m.anchor, np.int32), td(m.uniforms, np.float32)
+        toks = torch.empty(Rm, Gm, dtype=torch.int32, device=dev)
+        logits = torch.empty(Rm, Gm, Vm, dtype=torch.float32, device=dev)
+        nb = specv.specv_markov_draft_workspace_size(Rm, Gm, Vm, rank)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        call = lambda: check(specv.specv_markov_draft(U.data_ptr(), W1.data_ptr(), W2.data_ptr(), anchor.data_ptr(),
+                                                      u.data_ptr(), Rm, Gm, Vm, rank, 1.0, toks.data_ptr(),
+                                                      logits.data_ptr(), specv.SPECV_F32, ws.data_ptr(), nb, sp),
+                             "specv_markov_draft")
+        algo = Gm * (Rm * Vm * 2 + rank * Vm * 2 + Rm * Vm * 4)
+        flops = Gm * 2 * Rm * rank * Vm
+        units, unit, metric = Rm * Gm, "tokens/s", "Markov-head drafting: draft tokens/sec"
+        desc = "DSpark Markov head: R=512, gamma=7, V=129280, rank 256, T=1, float32 logits out"
+        launches, kernel = 2 * Gm, "markov logits + sample (whole call)"
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo,
+                "tensor_tflops": flops / (ms * 1e-3) / 1e12}
+    elif w == "schedule":
+        Rs, Gs = 512, 7
+        conf = td(synth.confidences(5, Rs, Gs))
+        sps = td(synth.sps_table(4096))
+        lengths = torch.empty(Rs, dtype=torch.int32, device=dev)
+        theta = torch.empty(1, dtype=torch.float64, device=dev)
+        nb = specv.specv_schedule_workspace_size(Rs, Gs)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        call = lambda: check(specv.specv_schedule(conf.data_ptr(), sps.data_ptr(), Rs, Gs, 4096, lengths.data_ptr(),
+                                                  theta.data_ptr(), ws.data_ptr(), ws.numel(), sp), "specv_schedule")
+        ms, clocks = _timed(call, None, args.steps, args.warmup, stream)
+        units, unit, metric = 1, "schedules/s", "greedy scheduler: schedules/sec (latency-bound)"
+        desc, launches, kernel = "scheduler: R=512, gamma=7, SPS table 4096 entries", 1, "schedule"
+        roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "traffic": None, "kernel": kernel}
+    else:
+        raise SystemExit(f"unknown workload {w}")
+    if roof.get("achieved") is not None:
+        roof["frac"] = roof["achieved"] / roof["peak"]
+    out = {"metric": metric, "value": units / (ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": desc, "l2": "flushed (2x L2 write) before every timed step"
+                      if w != "schedule" else "inputs are a few KB (L2-resident)"},
+           "roofline": roof, "gpu_launches": None if launches is None else launches * args.steps, "clocks": clocks}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     global R, ALGO_BYTES, WORKLOAD
     ap = argparse.ArgumentParser()
@@ -320,6 +477,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
+    ap.add_argument("--workload", default="chain", choices=["chain", "greedy", "tv", "tree", "markov", "schedule"])
     args = ap.parse_args()
     if args.requests != R:
         R = args.requests
@@ -327,6 +485,8 @@ def main():
         WORKLOAD = WORKLOAD.replace("R=64", f"R={R}")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "chain":
+        return run_workload(args)
     return run_ours(args)
 
 

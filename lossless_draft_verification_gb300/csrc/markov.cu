@@ -5,7 +5,18 @@
 // (W1 [V, r] used as a row lookup, W2 [r, V] as a logit projection), sampled
 // position by position from the anchor x_0.
 //
-// Per step k (x_{k-1} -> x_k):
+// Per step k (x_{k-1} -> x_k), tensor-core form (rank a multiple of 64, at most
+// 256; V a multiple of 8; 16-byte aligned tensors):
+//   markov_tc       persistent: one CTA per SM, each owning 256 requests (two
+//                   M = 128 blocks) and a strided set of 64-column vocabulary
+//                   tiles.  The W1[x_{k-1}] rows are gathered once into shared
+//                   memory (K-major, 128-byte swizzle); a TMA warp streams
+//                   tiles of W2^T (transposed once per call into the workspace)
+//                   through a two-stage ring; one thread issues tcgen05.mma
+//                   (M = 128, N = 64, K = 16, bf16 -> float32) into a
+//                   double-buffered TMEM accumulator; eight epilogue warps read
+//                   TMEM, add U_k, write L and the tile's softmax partials.
+// CUDA-core form (any other shape):
 //   markov_logits   L = U_k + W1[x_{k-1}] . W2 for a [BM x BN] output tile,
 //                   float32 accumulation; the epilogue writes L (float32 or
 //                   bf16) and the tile's softmax partials (max * c2,
@@ -13,12 +24,17 @@
 //   markov_sample   one warp per request: combines the tile partials, picks the
 //                   tile holding u * Z and rescans its BN logits (inverse CDF
 //                   over ascending ids), or takes the argmax at T = 0.
+#include <atomic>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "common.cuh"
 #include "host_common.h"
+#include "tc.cuh"
 
 namespace specv {
 
@@ -49,6 +65,7 @@ struct MarkovArgs {
   int ntile;
   float c2;                   // log2(e)/T, 0 at T = 0
   int greedy;
+  int tile_w;                 // vocabulary columns per partial (64 or 128)
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
@@ -219,13 +236,14 @@ __global__ void __launch_bounds__(128) markov_sample_kernel(MarkovArgs a) {
       const MarkovPart p = part[sel];
       const float s = ex2(p.a - M);
       const size_t rowbase = size_t(r) * a.lstride_r + a.step_off;
+      const int cpl = a.tile_w / 32;             // columns per lane: 2 or 4
       float w[4];
       float ls = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int v = sel * kMkBN + lane * 4 + c;
+        const int v = sel * a.tile_w + lane * cpl + c;
         float x = neg_inf();
-        if (v < a.V) {
+        if (c < cpl && v < a.V) {
           x = a.logits_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.logits)[rowbase + v])
                             : reinterpret_cast<const float*>(a.logits)[rowbase + v];
         }
@@ -237,8 +255,9 @@ __global__ void __launch_bounds__(128) markov_sample_kernel(MarkovArgs a) {
       int cand = 0x7fffffff, last = -1;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        if (c >= cpl) break;
         accv += w[c];
-        const int v = sel * kMkBN + lane * 4 + c;
+        const int v = sel * a.tile_w + lane * cpl + c;
         if (w[c] > 0.f) last = v;
         if (cand == 0x7fffffff && accv > target && w[c] > 0.f) cand = v;
       }
@@ -257,21 +276,286 @@ __global__ void __launch_bounds__(128) markov_sample_kernel(MarkovArgs a) {
   }
 }
 
-namespace {
-struct MarkovLayout {
-  size_t part_off, scratch_off, total;
-  int ntile;
+// ---------------------------------------------------------------------------
+// tensor-core form
+constexpr int kTcBN = 64;                 // vocabulary columns per tile (UMMA N)
+constexpr int kTcBM = 128;                // requests per M block (UMMA M)
+constexpr int kTcMB = 2;                  // M blocks per CTA
+constexpr int kTcMaxKC = 4;               // 64-wide rank chunks (rank <= 256)
+constexpr int kTcEpiWarps = 8;            // warp w: TMEM lane quarter w % 4, M block w / 4
+constexpr int kTcThreads = (kTcEpiWarps + 2) * 32;   // + TMA warp + MMA warp
+constexpr uint32_t kTcTmemCols = 256;     // 2 accumulator buffers x 2 M blocks x 64 columns
+constexpr uint32_t kTcRowBytes = 128;     // one swizzled row: 64 bf16 of K
+constexpr size_t kTcSmemE = size_t(kTcMB) * kTcMaxKC * kTcBM * kTcRowBytes;   // 128 KB
+constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * kTcBN * kTcRowBytes;       // 64 KB, two stages
+constexpr size_t kTcSmem = kTcSmemE + kTcSmemB + 1024;                        // + alignment slack
+constexpr uint32_t kTcMaxPolls = 1u << 22;   // bound on every mbarrier wait
+constexpr uint32_t kTcIdesc = tc::idesc_bf16_f32(kTcBM, kTcBN);
+
+struct MarkovTcArgs {
+  MarkovArgs m;
+  int nkc;          // rank / 64
+  int ntiles;       // ceil(V / 64)
+  int per_mp;       // CTAs per group of 256 requests
 };
-MarkovLayout markov_layout(int R, int V) {
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2t, MarkovTcArgs ta) {
+  const MarkovArgs& a = ta.m;
+  extern __shared__ uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_err;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = smem;                     // [M block][rank chunk][128 rows][128 B]
+  uint8_t* sB = smem + kTcSmemE;          // [stage][rank chunk][64 rows][128 B]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mp = blockIdx.x / ta.per_mp, j0 = blockIdx.x - (blockIdx.x / ta.per_mp) * ta.per_mp;
+  const int row0 = mp * (kTcMB * kTcBM);
+  const int nmb = min(kTcMB, (a.R - row0 + kTcBM - 1) / kTcBM);      // M blocks holding requests
+  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], kTcEpiWarps);
+    }
+    mbar_init(&bar_done, 1);
+    s_err = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
+  if (warp < kTcEpiWarps) {
+    // A operand: E[r, :] = W1[x_{k-1}(r), :] in the canonical K-major 128-byte-swizzle layout
+    for (int rr = threadIdx.x; rr < kTcMB * kTcBM; rr += kTcEpiWarps * 32) {
+      const int mb = rr / kTcBM, r = rr - (rr / kTcBM) * kTcBM;
+      const int req = row0 + rr;
+      int x = -1;
+      if (req < a.R) {
+        x = prev_token(a, req);
+        if (x < 0 || x >= a.V) x = -1;
+      }
+      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
+      for (int kc = 0; kc < ta.nkc; ++kc) {
+        uint8_t* dst = sE + (size_t(mb) * kTcMaxKC + kc) * (kTcBM * kTcRowBytes) + r * kTcRowBytes;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(dst + ((g ^ (r & 7)) << 4)) = v;
+        }
+      }
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kTcEpiWarps) {
+    // ---- TMA producer: W2^T rows [t*64, t*64+64) x rank, one 8 KB box per rank chunk
+    if (lane == 0) {
+      int i = 0;
+      for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
+        const int s = i & 1;
+        if (!mbar_wait_parity(&bar_empty[s], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        mbar_arrive_expect_tx(&bar_full[s], uint32_t(ta.nkc) * kTcBN * kTcRowBytes);
+        for (int kc = 0; kc < ta.nkc; ++kc)
+          tc::tma_load_2d(sB + (size_t(s) * kTcMaxKC + kc) * (kTcBN * kTcRowBytes), &tmap_w2t, kc * 64, t * kTcBN,
+                          &bar_full[s]);
+      }
+      // every issued copy has landed before the CTA may leave
+      for (int d = (i >= 2 ? i - 2 : 0); d < i; ++d)
+        if (!mbar_wait_parity(&bar_full[d & 1], (d >> 1) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      int i = 0;
+      for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
+        const int s = i & 1, b = i & 1;
+        if (!mbar_wait_parity(&bar_tempty[b], ((i >> 1) & 1) ^ 1, kTcMaxPolls) ||
+            !mbar_wait_parity(&bar_full[s], (i >> 1) & 1, kTcMaxPolls)) {
+          s_err = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t aE = smem_addr(sE), aB = smem_addr(sB) + uint32_t(s) * kTcMaxKC * kTcBN * kTcRowBytes;
+        for (int mb = 0; mb < nmb; ++mb)
+          for (int kk = 0; kk < ta.nkc * 4; ++kk) {
+            const uint64_t da = tc::smem_desc_k_sw128(aE + uint32_t(mb * kTcMaxKC + (kk >> 2)) * (kTcBM * kTcRowBytes) +
+                                                      uint32_t(kk & 3) * 32);
+            const uint64_t db = tc::smem_desc_k_sw128(aB + uint32_t(kk >> 2) * (kTcBN * kTcRowBytes) +
+                                                      uint32_t(kk & 3) * 32);
+            tc::mma_bf16(tmem + uint32_t(b * 128 + mb * 64), da, db, kTcIdesc, kk > 0 ? 1u : 0u);
+          }
+        tc::commit(&bar_empty[s]);            // the W2^T stage is free once these MMAs have read it
+        tc::commit(&bar_tfull[b]);            // the accumulators are ready for the epilogue
+      }
+      tc::commit(&bar_done);
+      if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
+    }
+  } else {
+    // ---- epilogue: L = U_k + acc, logits out, per-tile softmax partials
+    const int q = warp & 3, mb = warp >> 2;
+    const int r = row0 + mb * kTcBM + q * 32 + lane;
+    const bool rv = mb < nmb && r < a.R;
+    const uint4* urow = reinterpret_cast<const uint4*>(a.U + (size_t(r) * a.gamma + (a.k - 1)) * a.V);
+    const size_t lbase = size_t(r) * a.lstride_r + a.step_off;
+    int i = 0;
+    for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
+      const int b = i & 1;
+      const int n0 = t * kTcBN;
+      uint4 u[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) u[c] = (rv && n0 + 8 * c < a.V) ? __ldg(urow + (n0 >> 3) + c) : make_uint4(0u, 0u, 0u, 0u);
+      // warp-uniform outcome: tcgen05.ld below needs all 32 lanes
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[b], (i >> 1) & 1, kTcMaxPolls))) {
+        s_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      float acc0[32], acc1[32];
+      const uint32_t ta_ = tmem + (uint32_t(q * 32) << 16) + uint32_t(b * 128 + mb * 64);
+      tc::tmem_ld32(ta_, acc0);
+      tc::tmem_ld32(ta_ + 32, acc1);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tempty[b]);
+      if (!rv) continue;
+      float L[64];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t wv[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = 8 * c + e;
+          const float ub = __uint_as_float(e & 1 ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16));
+          float x = ub + (j < 32 ? acc0[j] : acc1[j - 32]);
+          if (a.logits_bf16) x = round_to_bf16(x);
+          L[j] = n0 + j < a.V ? x : neg_inf();
+        }
+      }
+      if (a.logits) {
+        if (a.logits_bf16) {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(a.logits) + lbase + n0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (n0 + 8 * c < a.V) {
+              uint4 o;
+              o.x = (__float_as_uint(L[8 * c + 0]) >> 16) | (__float_as_uint(L[8 * c + 1]) & 0xFFFF0000u);
+              o.y = (__float_as_uint(L[8 * c + 2]) >> 16) | (__float_as_uint(L[8 * c + 3]) & 0xFFFF0000u);
+              o.z = (__float_as_uint(L[8 * c + 4]) >> 16) | (__float_as_uint(L[8 * c + 5]) & 0xFFFF0000u);
+              o.w = (__float_as_uint(L[8 * c + 6]) >> 16) | (__float_as_uint(L[8 * c + 7]) & 0xFFFF0000u);
+              *reinterpret_cast<uint4*>(dst + 8 * c) = o;
+            }
+        } else {
+          float* dst = reinterpret_cast<float*>(a.logits) + lbase + n0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (n0 + 4 * c < a.V)
+              __stcs(reinterpret_cast<float4*>(dst + 4 * c), make_float4(L[4 * c], L[4 * c + 1], L[4 * c + 2], L[4 * c + 3]));
+        }
+      }
+      MarkovPart mpart;
+      if (a.greedy) {
+        float m = L[0];
+        int idx = n0;
+#pragma unroll
+        for (int j = 1; j < 64; ++j)
+          if (L[j] > m) { m = L[j]; idx = n0 + j; }
+        mpart.a = m;
+        mpart.b = __int_as_float(idx);
+      } else {
+        float m = L[0];
+#pragma unroll
+        for (int j = 1; j < 64; ++j) m = fmaxf(m, L[j]);
+        const float m_c2 = m * a.c2;
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          z0 += ex2(fmaf(L[j], a.c2, -m_c2));
+          z1 += ex2(fmaf(L[j + 1], a.c2, -m_c2));
+        }
+        mpart.a = m_c2;
+        mpart.b = z0 + z1;
+      }
+      a.part[size_t(r) * a.ntile + t] = mpart;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kTcEpiWarps + 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTcTmemCols);
+  }
+  if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+}
+
+// W2 [rank, V] -> W2^T [V, rank], 64 x 64 tiles through shared memory
+__global__ void __launch_bounds__(256) transpose_w2_kernel(const uint16_t* __restrict__ W2, uint16_t* __restrict__ W2T,
+                                                           int rank, int V) {
+  __shared__ uint16_t t[64][66];
+  const int v0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;    // 64 x 4
+  for (int i = ty; i < 64; i += 4) {
+    const int j = j0 + i, v = v0 + tx;
+    t[i][tx] = (j < rank && v < V) ? W2[size_t(j) * V + v] : uint16_t(0);
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 4) {
+    const int v = v0 + i, j = j0 + tx;
+    if (v < V && j < rank) W2T[size_t(v) * rank + j] = t[tx][i];
+  }
+}
+
+namespace {
+// Workspace: header | tile partials [R, ceil(V / 64)] | float32 logits [R, V]
+// (when the caller keeps none) | W2^T [V, rank] bf16 (tensor-core form)
+struct MarkovLayout {
+  size_t part_off, scratch_off, w2t_off, total;
+};
+MarkovLayout markov_layout(int R, int V, int rank) {
   MarkovLayout L;
-  L.ntile = (V + kMkBN - 1) / kMkBN;
   size_t off = kHeaderBytes;
   L.part_off = off;
-  off = align256(off + size_t(R) * L.ntile * sizeof(MarkovPart));
+  off = align256(off + size_t(R) * ((V + kTcBN - 1) / kTcBN) * sizeof(MarkovPart));
   L.scratch_off = off;
   off = align256(off + size_t(R) * V * sizeof(float));
+  L.w2t_off = off;
+  if (rank % 64 == 0 && rank <= kTcMaxKC * 64 && V % 8 == 0) off = align256(off + size_t(V) * rank * 2);
   L.total = off;
   return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* p = fn.load(std::memory_order_acquire);
+  if (p == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+      return nullptr;
+    fn.store(p, std::memory_order_release);
+  }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+}
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 }  // namespace
 
@@ -281,7 +565,7 @@ using namespace specv;
 
 extern "C" size_t specv_markov_draft_workspace_size(int R, int gamma, int V, int rank) {
   if (R < 0 || gamma < 0 || V < 1 || rank < 1 || rank > SPECV_MAX_MARKOV_RANK) return 0;
-  return markov_layout(R, V).total;
+  return markov_layout(R, V, rank).total;
 }
 
 extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const void* W2, const int32_t* anchor,
@@ -300,7 +584,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       !aligned_to(uniforms, 4) || !aligned_to(draft_tokens, 4) || !aligned_to(workspace, 256) ||
       !aligned_to(draft_logits, logits_out_dtype == SPECV_BF16 ? 2 : 4))
     return SPECV_ERR_INVALID_ARG;
-  const MarkovLayout L = markov_layout(R, V);
+  const MarkovLayout L = markov_layout(R, V, rank);
   if (workspace_bytes < L.total) return SPECV_ERR_INVALID_ARG;
   specv_status s = check_device();
   if (s != SPECV_OK) return s;
@@ -328,10 +612,58 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
   a.gamma = gamma;
   a.V = V;
   a.rank = rank;
-  a.ntile = L.ntile;
   a.greedy = temperature == 0.f;
   a.c2 = a.greedy ? 0.f : kLog2e / temperature;
-  const dim3 g1(unsigned(L.ntile), unsigned((R + kMkBM - 1) / kMkBM));
+  const bool tc_shape = rank % 64 == 0 && rank <= kTcMaxKC * 64 && V % 8 == 0 && aligned_to(U, 16) &&
+                        aligned_to(W1, 16) && (!draft_logits || aligned_to(draft_logits, 16));
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tc_shape ? tensor_map_encoder() : nullptr;
+  const int nsm = sm_count();
+  if (encode != nullptr && nsm > 0) {
+    // tensor-core form: W2^T once, then per step the GEMM + epilogue and the sampler
+    uint16_t* w2t = reinterpret_cast<uint16_t*>(base + L.w2t_off);
+    const dim3 gt(unsigned((V + 63) / 64), unsigned((rank + 63) / 64));
+    const uint16_t* w2 = a.W2;
+    void* xargs[] = {&w2, &w2t, &rank, &V};
+    if (cudaLaunchKernel(reinterpret_cast<void*>(&transpose_w2_kernel), gt, dim3(256), xargs, 0, st) != cudaSuccess)
+      return SPECV_ERR_CUDA;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {cuuint64_t(rank), cuuint64_t(V)};
+    const cuuint64_t gstride[1] = {cuuint64_t(rank) * 2};
+    const cuuint32_t box[2] = {64, uint32_t(kTcBN)};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w2t, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPECV_ERR_CUDA;
+    if (cudaFuncSetAttribute(reinterpret_cast<void*>(&markov_tc_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTcSmem)) != cudaSuccess)
+      return SPECV_ERR_CUDA;
+    MarkovTcArgs ta;
+    a.tile_w = kTcBN;
+    a.ntile = (V + kTcBN - 1) / kTcBN;
+    ta.nkc = rank / 64;
+    ta.ntiles = a.ntile;
+    const int n_mp = (R + kTcMB * kTcBM - 1) / (kTcMB * kTcBM);
+    ta.per_mp = nsm / n_mp > 0 ? nsm / n_mp : 1;
+    const dim3 g1(unsigned(n_mp * ta.per_mp));
+    const dim3 g2(unsigned((R + 3) / 4));
+    for (int k = 1; k <= gamma; ++k) {
+      a.k = k;
+      a.step_off = draft_logits ? long(k - 1) * V : 0;
+      ta.m = a;
+      void* targs[] = {&tmap, &ta};
+      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_tc_kernel), g1, dim3(kTcThreads), targs, kTcSmem, st) !=
+          cudaSuccess)
+        return SPECV_ERR_CUDA;
+      void* sargs[] = {&a};
+      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), g2, dim3(128), sargs, 0, st) != cudaSuccess)
+        return SPECV_ERR_CUDA;
+    }
+    return SPECV_OK;
+  }
+  a.tile_w = kMkBN;
+  a.ntile = (V + kMkBN - 1) / kMkBN;
+  const dim3 g1(unsigned(a.ntile), unsigned((R + kMkBM - 1) / kMkBM));
   const dim3 g2(unsigned((R + 3) / 4));
   for (int k = 1; k <= gamma; ++k) {
     a.k = k;
