@@ -183,92 +183,160 @@ __global__ void __launch_bounds__(kMkThreads) markov_logits_kernel(MarkovArgs a)
   }
 }
 
-__global__ void __launch_bounds__(128) markov_sample_kernel(MarkovArgs a) {
+// One CTA per request: combine the tile partials, pick the tile holding u * Z
+// (prefix over tiles in index order), rescan its logits; T = 0 takes the argmax.
+constexpr int kSampleThreads = 256;
+constexpr int kSampleWarps = kSampleThreads / 32;
+
+__global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArgs a) {
+  __shared__ float s_f[kSampleWarps];
+  __shared__ int s_i[kSampleWarps];
+  __shared__ int s_sel;
+  __shared__ float s_base, s_target, s_M;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 4 + warp;
-  if (r >= a.R) return;
+  const int r = blockIdx.x;
   const int x_prev = prev_token(a, r);
   const MarkovPart* part = a.part + size_t(r) * a.ntile;
-  int tok = -1;
-  bool bad = x_prev < 0 || x_prev >= a.V;
   const float u = a.greedy ? 0.f : a.uniforms[size_t(r) * a.gamma + (a.k - 1)];
-  if (!a.greedy && !(u >= 0.f && u < 1.f)) bad = true;
-  if (!bad && a.greedy) {
+  const bool bad_in = x_prev < 0 || x_prev >= a.V || (!a.greedy && !(u >= 0.f && u < 1.f));
+  int tok = -1;
+  if (a.greedy) {
     float v = neg_inf();
     int i = 0x7fffffff;
-    for (int t = lane; t < a.ntile; t += 32) {
+    for (int t = threadIdx.x; t < a.ntile; t += kSampleThreads) {
       const MarkovPart p = part[t];
       const int pi = __float_as_int(p.b);
       if (p.a > v || (p.a == v && pi < i)) { v = p.a; i = pi; }
     }
     warp_argmax(v, i);
-    tok = i;
-  } else if (!bad) {
-    float M = neg_inf();
-    for (int t = lane; t < a.ntile; t += 32) M = fmaxf(M, part[t].a);
-    M = warp_max(M);
-    const int per = (a.ntile + 31) / 32;
-    const int t0 = lane * per, t1 = min(a.ntile, t0 + per);
-    float lsum = 0.f;
-    for (int t = t0; t < t1; ++t) lsum += part[t].b * ex2(part[t].a - M);
-    const float incl = warp_inclusive_scan(lsum);
-    const float total = __shfl_sync(0xffffffffu, incl, 31);
-    const float target = u * total;
-    const unsigned hit = __ballot_sync(0xffffffffu, incl > target && t1 > t0);
+    if (lane == 0) { s_f[warp] = v; s_i[warp] = i; }
+    __syncthreads();
+    if (warp == 0) {
+      v = lane < kSampleWarps ? s_f[lane] : neg_inf();
+      i = lane < kSampleWarps ? s_i[lane] : 0x7fffffff;
+      warp_argmax(v, i);
+      if (lane == 0) {
+        a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad_in ? -1 : i;
+        if (bad_in) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
+      }
+    }
+    return;
+  }
+  // row maximum of the tile maxima (already times c2)
+  float M = neg_inf();
+  for (int t = threadIdx.x; t < a.ntile; t += kSampleThreads) M = fmaxf(M, part[t].a);
+  M = warp_max(M);
+  if (lane == 0) s_f[warp] = M;
+  __syncthreads();
+  if (warp == 0) {
+    float m = lane < kSampleWarps ? s_f[lane] : neg_inf();
+    m = warp_max(m);
+    if (lane == 0) s_M = m;
+  }
+  __syncthreads();
+  M = s_M;
+  // each thread: a contiguous run of tiles; block-wide inclusive scan of the masses
+  const int per = (a.ntile + kSampleThreads - 1) / kSampleThreads;
+  const int t0 = threadIdx.x * per, t1 = min(a.ntile, t0 + per);
+  float lsum = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const MarkovPart p = part[t];
+    lsum += p.b * ex2(p.a - M);
+  }
+  float incl = warp_inclusive_scan(lsum);
+  if (lane == 31) s_f[warp] = incl;
+  __syncthreads();
+  float wpre = 0.f, total = 0.f;
+#pragma unroll
+  for (int w = 0; w < kSampleWarps; ++w) {
+    const float x = s_f[w];
+    if (w < warp) wpre += x;
+    total += x;
+  }
+  incl += wpre;
+  const float target = u * total;
+  if (threadIdx.x == 0) {
+    s_sel = -1;
+    s_target = target;
+  }
+  __syncthreads();
+  // first thread whose run passes the target; it walks its run (rounding may
+  // leave none: then the last thread with mass takes its last tile with mass)
+  const bool hit = incl > target && t1 > t0 && lsum > 0.f;
+  const unsigned wb = __ballot_sync(0xffffffffu, hit);
+  if (lane == 0) s_i[warp] = wb ? warp * 32 + __ffs(wb) - 1 : 0x7fffffff;
+  __syncthreads();
+  int first = 0x7fffffff;
+#pragma unroll
+  for (int w = 0; w < kSampleWarps; ++w) first = min(first, s_i[w]);
+  if (first == 0x7fffffff) {                      // block-uniform
+    __syncthreads();                               // every thread has read s_i
+    const unsigned mb = __ballot_sync(0xffffffffu, lsum > 0.f);
+    if (lane == 0) s_i[warp] = mb ? warp * 32 + 31 - __clz(mb) : -1;
+    __syncthreads();
+    int last = -1;
+#pragma unroll
+    for (int w = 0; w < kSampleWarps; ++w) last = max(last, s_i[w]);
+    first = last;
+  }
+  if (int(threadIdx.x) == first) {
+    float run = incl - lsum;
     int sel = -1;
     float base = 0.f;
-    const int L = hit ? __ffs(hit) - 1 : 31;
-    if (lane == L) {
-      float run = incl - lsum;
-      for (int t = t0; t < t1; ++t) {
-        const float m = part[t].b * ex2(part[t].a - M);
-        if (hit && run + m > target && m > 0.f) { sel = t; base = run; break; }
-        if (!hit && m > 0.f) { sel = t; base = run; }
-        run += m;
+    for (int t = t0; t < t1; ++t) {
+      const MarkovPart p = part[t];
+      const float m = p.b * ex2(p.a - M);
+      if (m > 0.f) {
+        sel = t;
+        base = run;
+        if (run + m > target) break;
       }
+      run += m;
     }
-    sel = __shfl_sync(0xffffffffu, sel, L);
-    base = __shfl_sync(0xffffffffu, base, L);
-    if (sel < 0) {
-      bad = true;
-    } else {
-      // rescan the selected tile's columns in index order
-      const MarkovPart p = part[sel];
-      const float s = ex2(p.a - M);
-      const size_t rowbase = size_t(r) * a.lstride_r + a.step_off;
-      const int cpl = a.tile_w / 32;             // columns per lane: 2 or 4
-      float w[4];
-      float ls = 0.f;
+    s_sel = sel;
+    s_base = base;
+  }
+  __syncthreads();
+  const int sel = s_sel;
+  if (warp != 0) return;
+  bool bad = bad_in || sel < 0;
+  if (!bad) {
+    // rescan the selected tile's columns in index order
+    const MarkovPart p = part[sel];
+    const float sc = ex2(p.a - M);
+    const size_t rowbase = size_t(r) * a.lstride_r + a.step_off;
+    const int cpl = a.tile_w / 32;             // columns per lane: 2 or 4
+    float w[4];
+    float ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int v = sel * a.tile_w + lane * cpl + c;
-        float x = neg_inf();
-        if (c < cpl && v < a.V) {
-          x = a.logits_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.logits)[rowbase + v])
-                            : reinterpret_cast<const float*>(a.logits)[rowbase + v];
-        }
-        w[c] = __fmul_rn(ex2(fmaf(x, a.c2, -p.a)), s);
-        ls += w[c];
+    for (int c = 0; c < 4; ++c) {
+      const int v = sel * a.tile_w + lane * cpl + c;
+      float x = neg_inf();
+      if (c < cpl && v < a.V) {
+        x = a.logits_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.logits)[rowbase + v])
+                          : reinterpret_cast<const float*>(a.logits)[rowbase + v];
       }
-      const float inc = warp_inclusive_scan(ls);
-      float accv = base + (inc - ls);
-      int cand = 0x7fffffff, last = -1;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c >= cpl) break;
-        accv += w[c];
-        const int v = sel * a.tile_w + lane * cpl + c;
-        if (w[c] > 0.f) last = v;
-        if (cand == 0x7fffffff && accv > target && w[c] > 0.f) cand = v;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-      }
-      tok = cand != 0x7fffffff ? cand : last;
-      if (tok < 0) bad = true;
+      w[c] = __fmul_rn(ex2(fmaf(x, a.c2, -p.a)), sc);
+      ls += w[c];
     }
+    const float inc = warp_inclusive_scan(ls);
+    float accv = s_base + (inc - ls);
+    int cand = 0x7fffffff, last = -1;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c >= cpl) break;
+      accv += w[c];
+      const int v = sel * a.tile_w + lane * cpl + c;
+      if (w[c] > 0.f) last = v;
+      if (cand == 0x7fffffff && accv > s_target && w[c] > 0.f) cand = v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+      last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    }
+    tok = cand != 0x7fffffff ? cand : last;
+    if (tok < 0) bad = true;
   }
   if (lane == 0) {
     a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad ? -1 : tok;
@@ -279,16 +347,17 @@ __global__ void __launch_bounds__(128) markov_sample_kernel(MarkovArgs a) {
 // ---------------------------------------------------------------------------
 // tensor-core form
 constexpr int kTcBN = 64;                 // vocabulary columns per tile (UMMA N)
-constexpr int kTcBM = 128;                // requests per M block (UMMA M)
-constexpr int kTcMB = 2;                  // M blocks per CTA
+constexpr int kTcBM = 128;                // requests per CTA (UMMA M)
 constexpr int kTcMaxKC = 4;               // 64-wide rank chunks (rank <= 256)
-constexpr int kTcEpiWarps = 8;            // warp w: TMEM lane quarter w % 4, M block w / 4
+constexpr int kTcEpiWarps = 8;            // two groups of four: group g takes the tiles i with i % 2 == g
 constexpr int kTcThreads = (kTcEpiWarps + 2) * 32;   // + TMA warp + MMA warp
-constexpr uint32_t kTcTmemCols = 256;     // 2 accumulator buffers x 2 M blocks x 64 columns
-constexpr uint32_t kTcRowBytes = 128;     // one swizzled row: 64 bf16 of K
-constexpr size_t kTcSmemE = size_t(kTcMB) * kTcMaxKC * kTcBM * kTcRowBytes;   // 128 KB
-constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * kTcBN * kTcRowBytes;       // 64 KB, two stages
-constexpr size_t kTcSmem = kTcSmemE + kTcSmemB + 1024;                        // + alignment slack
+constexpr uint32_t kTcTmemCols = 128;     // two accumulator buffers of 64 columns
+constexpr uint32_t kTcRowBytes = 128;     // one swizzled row
+constexpr size_t kTcSmemE = size_t(kTcMaxKC) * kTcBM * kTcRowBytes;        // 64 KB: W1 rows
+constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * kTcBN * kTcRowBytes;    // 64 KB: W2^T, two stages
+constexpr size_t kTcSmemU = size_t(2) * kTcBM * kTcRowBytes;               // 32 KB: U tiles, two stages
+constexpr size_t kTcSmemL = size_t(kTcEpiWarps) * 2 * 32 * kTcRowBytes;    // 64 KB: logit staging per warp
+constexpr size_t kTcSmem = kTcSmemE + kTcSmemB + kTcSmemU + kTcSmemL + 1024;
 constexpr uint32_t kTcMaxPolls = 1u << 22;   // bound on every mbarrier wait
 constexpr uint32_t kTcIdesc = tc::idesc_bf16_f32(kTcBM, kTcBN);
 
@@ -296,24 +365,31 @@ struct MarkovTcArgs {
   MarkovArgs m;
   int nkc;          // rank / 64
   int ntiles;       // ceil(V / 64)
-  int per_mp;       // CTAs per group of 256 requests
+  int per_mb;       // CTAs per 128-request block
+  int lz;           // logits tensor map: z coordinate = request, y = step slot
 };
 
+// 16-byte granule g of row r in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128(int r, int g) { return uint32_t(r) * kTcRowBytes + (uint32_t(g ^ (r & 7)) << 4); }
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-    markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2t, MarkovTcArgs ta) {
+    markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2t, const __grid_constant__ CUtensorMap tmap_u,
+                     const __grid_constant__ CUtensorMap tmap_l, MarkovTcArgs ta) {
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
-  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_tfull[2], bar_tempty[2], bar_ufull[2], bar_uempty[2],
+      bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_err;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sE = smem;                     // [M block][rank chunk][128 rows][128 B]
-  uint8_t* sB = smem + kTcSmemE;          // [stage][rank chunk][64 rows][128 B]
+  uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
+  uint8_t* sB = sE + kTcSmemE;                      // [stage][rank chunk][64 rows][128 B]
+  uint8_t* sU = sB + kTcSmemB;                      // [stage][128 rows][128 B]  (64 bf16 per row)
+  uint8_t* sL = sU + kTcSmemU;                      // [warp][2 halves][32 rows][128 B]  (32 floats per row)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mp = blockIdx.x / ta.per_mp, j0 = blockIdx.x - (blockIdx.x / ta.per_mp) * ta.per_mp;
-  const int row0 = mp * (kTcMB * kTcBM);
-  const int nmb = min(kTcMB, (a.R - row0 + kTcBM - 1) / kTcBM);      // M blocks holding requests
+  const int mb = blockIdx.x / ta.per_mb, j0 = blockIdx.x - (blockIdx.x / ta.per_mb) * ta.per_mb;
+  const int row0 = mb * kTcBM;
   if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
   if (threadIdx.x == 0) {
@@ -321,7 +397,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
       mbar_init(&bar_tfull[i], 1);
-      mbar_init(&bar_tempty[i], kTcEpiWarps);
+      mbar_init(&bar_tempty[i], 4);
+      mbar_init(&bar_ufull[i], 1);
+      mbar_init(&bar_uempty[i], 4);
     }
     mbar_init(&bar_done, 1);
     s_err = 0;
@@ -329,10 +407,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
   if (warp < kTcEpiWarps) {
-    // A operand: E[r, :] = W1[x_{k-1}(r), :] in the canonical K-major 128-byte-swizzle layout
-    for (int rr = threadIdx.x; rr < kTcMB * kTcBM; rr += kTcEpiWarps * 32) {
-      const int mb = rr / kTcBM, r = rr - (rr / kTcBM) * kTcBM;
-      const int req = row0 + rr;
+    // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
+    for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
+      const int req = row0 + r;
       int x = -1;
       if (req < a.R) {
         x = prev_token(a, req);
@@ -340,12 +417,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
       for (int kc = 0; kc < ta.nkc; ++kc) {
-        uint8_t* dst = sE + (size_t(mb) * kTcMaxKC + kc) * (kTcBM * kTcRowBytes) + r * kTcRowBytes;
+        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint4 v = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(dst + ((g ^ (r & 7)) << 4)) = v;
-        }
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(dst + sw128(r, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
       }
     }
     tc::fence_proxy_async_smem();
@@ -356,77 +431,84 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == kTcEpiWarps) {
-    // ---- TMA producer: W2^T rows [t*64, t*64+64) x rank, one 8 KB box per rank chunk
+    // ---- TMA producer: W2^T rows [t*64, t*64+64) (MMA operand) and U_k[rows, t*64 .. +64) (epilogue)
     if (lane == 0) {
       int i = 0;
-      for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
+      for (int t = j0; t < ta.ntiles; t += ta.per_mb, ++i) {
         const int s = i & 1;
-        if (!mbar_wait_parity(&bar_empty[s], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        const uint32_t fresh = ((i >> 1) & 1) ^ 1;
+        if (!mbar_wait_parity(&bar_empty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
         mbar_arrive_expect_tx(&bar_full[s], uint32_t(ta.nkc) * kTcBN * kTcRowBytes);
         for (int kc = 0; kc < ta.nkc; ++kc)
           tc::tma_load_2d(sB + (size_t(s) * kTcMaxKC + kc) * (kTcBN * kTcRowBytes), &tmap_w2t, kc * 64, t * kTcBN,
                           &bar_full[s]);
+        if (!mbar_wait_parity(&bar_uempty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
+        mbar_arrive_expect_tx(&bar_ufull[s], kTcBM * kTcRowBytes);
+        tc::tma_load_3d(sU + size_t(s) * (kTcBM * kTcRowBytes), &tmap_u, t * kTcBN, a.k - 1, row0, &bar_ufull[s]);
       }
       // every issued copy has landed before the CTA may leave
-      for (int d = (i >= 2 ? i - 2 : 0); d < i; ++d)
+      for (int d = (i >= 2 ? i - 2 : 0); d < i; ++d) {
         if (!mbar_wait_parity(&bar_full[d & 1], (d >> 1) & 1, kTcMaxPolls)) s_err = 1;
+        if (!mbar_wait_parity(&bar_ufull[d & 1], (d >> 1) & 1, kTcMaxPolls)) s_err = 1;
+      }
     }
   } else if (warp == kTcEpiWarps + 1) {
     // ---- MMA issuer
     if (lane == 0) {
       int i = 0;
-      for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
-        const int s = i & 1, b = i & 1;
-        if (!mbar_wait_parity(&bar_tempty[b], ((i >> 1) & 1) ^ 1, kTcMaxPolls) ||
+      for (int t = j0; t < ta.ntiles; t += ta.per_mb, ++i) {
+        const int s = i & 1;
+        if (!mbar_wait_parity(&bar_tempty[s], ((i >> 1) & 1) ^ 1, kTcMaxPolls) ||
             !mbar_wait_parity(&bar_full[s], (i >> 1) & 1, kTcMaxPolls)) {
           s_err = 1;
           break;
         }
         tc::fence_after_sync();
         const uint32_t aE = smem_addr(sE), aB = smem_addr(sB) + uint32_t(s) * kTcMaxKC * kTcBN * kTcRowBytes;
-        for (int mb = 0; mb < nmb; ++mb)
-          for (int kk = 0; kk < ta.nkc * 4; ++kk) {
-            const uint64_t da = tc::smem_desc_k_sw128(aE + uint32_t(mb * kTcMaxKC + (kk >> 2)) * (kTcBM * kTcRowBytes) +
-                                                      uint32_t(kk & 3) * 32);
-            const uint64_t db = tc::smem_desc_k_sw128(aB + uint32_t(kk >> 2) * (kTcBN * kTcRowBytes) +
-                                                      uint32_t(kk & 3) * 32);
-            tc::mma_bf16(tmem + uint32_t(b * 128 + mb * 64), da, db, kTcIdesc, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < ta.nkc * 4; ++kk) {
+          const uint64_t da = tc::smem_desc_k_sw128(aE + uint32_t(kk >> 2) * (kTcBM * kTcRowBytes) + uint32_t(kk & 3) * 32);
+          const uint64_t db = tc::smem_desc_k_sw128(aB + uint32_t(kk >> 2) * (kTcBN * kTcRowBytes) + uint32_t(kk & 3) * 32);
+          tc::mma_bf16(tmem + uint32_t(s * kTcBN), da, db, kTcIdesc, kk > 0 ? 1u : 0u);
+        }
         tc::commit(&bar_empty[s]);            // the W2^T stage is free once these MMAs have read it
-        tc::commit(&bar_tfull[b]);            // the accumulators are ready for the epilogue
+        tc::commit(&bar_tfull[s]);            // the accumulator is ready for the epilogue
       }
       tc::commit(&bar_done);
       if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
     }
   } else {
-    // ---- epilogue: L = U_k + acc, logits out, per-tile softmax partials
-    const int q = warp & 3, mb = warp >> 2;
-    const int r = row0 + mb * kTcBM + q * 32 + lane;
-    const bool rv = mb < nmb && r < a.R;
-    const uint4* urow = reinterpret_cast<const uint4*>(a.U + (size_t(r) * a.gamma + (a.k - 1)) * a.V);
-    const size_t lbase = size_t(r) * a.lstride_r + a.step_off;
-    int i = 0;
-    for (int t = j0; t < ta.ntiles; t += ta.per_mp, ++i) {
-      const int b = i & 1;
+    // ---- epilogue group g = warp / 4 takes tiles i = g, g + 2, ...; thread = request row
+    const int g = warp >> 2, qd = warp & 3;
+    const int rl = qd * 32 + lane;                  // row inside the 128-request block
+    const int r = row0 + rl;
+    const bool rv = r < a.R;
+    uint8_t* stage = sL + size_t(warp) * (2 * 32 * kTcRowBytes);
+    int i = g;
+    for (int t = j0 + g * ta.per_mb; t < ta.ntiles; t += 2 * ta.per_mb, i += 2) {
       const int n0 = t * kTcBN;
-      uint4 u[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) u[c] = (rv && n0 + 8 * c < a.V) ? __ldg(urow + (n0 >> 3) + c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t ph = (i >> 1) & 1;
       // warp-uniform outcome: tcgen05.ld below needs all 32 lanes
-      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[b], (i >> 1) & 1, kTcMaxPolls))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], ph, kTcMaxPolls) &&
+                                       mbar_wait_parity(&bar_ufull[g], ph, kTcMaxPolls))) {
         s_err = 1;
         break;
       }
       tc::fence_after_sync();
       float acc0[32], acc1[32];
-      const uint32_t ta_ = tmem + (uint32_t(q * 32) << 16) + uint32_t(b * 128 + mb * 64);
-      tc::tmem_ld32(ta_, acc0);
-      tc::tmem_ld32(ta_ + 32, acc1);
+      const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(g * kTcBN);
+      tc::tmem_ld32(taddr, acc0);
+      tc::tmem_ld32(taddr + 32, acc1);
       tc::tmem_ld_wait();
+      uint4 u[8];
+      const uint8_t* urow = sU + size_t(g) * (kTcBM * kTcRowBytes);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4*>(urow + sw128(rl, c));
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_tempty[b]);
-      if (!rv) continue;
+      if (lane == 0) {
+        mbar_arrive(&bar_tempty[g]);
+        mbar_arrive(&bar_uempty[g]);
+      }
       float L[64];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -440,27 +522,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           L[j] = n0 + j < a.V ? x : neg_inf();
         }
       }
-      if (a.logits) {
-        if (a.logits_bf16) {
-          uint16_t* dst = reinterpret_cast<uint16_t*>(a.logits) + lbase + n0;
+      // logits: this warp's 32 rows x 64 columns through swizzled staging, then TMA stores
+      if (lane == 0) tc::bulk_wait_read_all();     // the previous tile's stores have read the staging
+      __syncwarp();
+      if (a.logits_bf16) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (n0 + 8 * c < a.V) {
-              uint4 o;
-              o.x = (__float_as_uint(L[8 * c + 0]) >> 16) | (__float_as_uint(L[8 * c + 1]) & 0xFFFF0000u);
-              o.y = (__float_as_uint(L[8 * c + 2]) >> 16) | (__float_as_uint(L[8 * c + 3]) & 0xFFFF0000u);
-              o.z = (__float_as_uint(L[8 * c + 4]) >> 16) | (__float_as_uint(L[8 * c + 5]) & 0xFFFF0000u);
-              o.w = (__float_as_uint(L[8 * c + 6]) >> 16) | (__float_as_uint(L[8 * c + 7]) & 0xFFFF0000u);
-              *reinterpret_cast<uint4*>(dst + 8 * c) = o;
-            }
-        } else {
-          float* dst = reinterpret_cast<float*>(a.logits) + lbase + n0;
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (n0 + 4 * c < a.V)
-              __stcs(reinterpret_cast<float4*>(dst + 4 * c), make_float4(L[4 * c], L[4 * c + 1], L[4 * c + 2], L[4 * c + 3]));
+        for (int c = 0; c < 8; ++c) {
+          uint4 o;
+          o.x = (__float_as_uint(L[8 * c + 0]) >> 16) | (__float_as_uint(L[8 * c + 1]) & 0xFFFF0000u);
+          o.y = (__float_as_uint(L[8 * c + 2]) >> 16) | (__float_as_uint(L[8 * c + 3]) & 0xFFFF0000u);
+          o.z = (__float_as_uint(L[8 * c + 4]) >> 16) | (__float_as_uint(L[8 * c + 5]) & 0xFFFF0000u);
+          o.w = (__float_as_uint(L[8 * c + 6]) >> 16) | (__float_as_uint(L[8 * c + 7]) & 0xFFFF0000u);
+          *reinterpret_cast<uint4*>(stage + sw128(lane, c)) = o;
         }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<float4*>(stage + (c >> 3) * (32 * kTcRowBytes) + sw128(lane, c & 7)) =
+              make_float4(L[4 * c], L[4 * c + 1], L[4 * c + 2], L[4 * c + 3]);
       }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int z = row0 + qd * 32;
+        if (a.logits_bf16) {
+          tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
+        } else {
+          tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
+          tc::tma_store_3d(&tmap_l, n0 + 32, ta.lz, z, stage + 32 * kTcRowBytes);
+        }
+        tc::bulk_commit();
+      }
+      if (!rv) continue;
       MarkovPart mpart;
       if (a.greedy) {
         float m = L[0];
@@ -486,6 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       a.part[size_t(r) * a.ntile + t] = mpart;
     }
+    if (lane == 0) tc::bulk_wait_all();           // logits written before the sampler reads them
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -496,20 +590,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
 }
 
-// W2 [rank, V] -> W2^T [V, rank], 64 x 64 tiles through shared memory
+// W2 [rank, V] -> W2^T [V, rank]: 64 x 64 tiles through shared memory, two
+// bf16 per 32-bit access
 __global__ void __launch_bounds__(256) transpose_w2_kernel(const uint16_t* __restrict__ W2, uint16_t* __restrict__ W2T,
                                                            int rank, int V) {
   __shared__ uint16_t t[64][66];
   const int v0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;    // 64 x 4
-  for (int i = ty; i < 64; i += 4) {
-    const int j = j0 + i, v = v0 + tx;
-    t[i][tx] = (j < rank && v < V) ? W2[size_t(j) * V + v] : uint16_t(0);
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;    // 32 x 8
+  for (int i = ty; i < 64; i += 8) {
+    const int j = j0 + i, v = v0 + 2 * tx;
+    uint32_t w = 0;
+    if (j < rank && v + 1 < V) w = __ldg(reinterpret_cast<const uint32_t*>(W2 + size_t(j) * V + v));
+    else if (j < rank && v < V) w = W2[size_t(j) * V + v];
+    t[i][2 * tx] = uint16_t(w);
+    t[i][2 * tx + 1] = uint16_t(w >> 16);
   }
   __syncthreads();
-  for (int i = ty; i < 64; i += 4) {
-    const int v = v0 + i, j = j0 + tx;
-    if (v < V && j < rank) W2T[size_t(v) * rank + j] = t[tx][i];
+  for (int i = ty; i < 64; i += 8) {
+    const int v = v0 + i, j = j0 + 2 * tx;
+    if (v < V && j + 1 < rank)
+      *reinterpret_cast<uint32_t*>(W2T + size_t(v) * rank + j) = uint32_t(t[2 * tx][i]) | (uint32_t(t[2 * tx + 1][i]) << 16);
+    else if (v < V && j < rank)
+      W2T[size_t(v) * rank + j] = t[2 * tx][i];
   }
 }
 
@@ -626,15 +728,41 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     void* xargs[] = {&w2, &w2t, &rank, &V};
     if (cudaLaunchKernel(reinterpret_cast<void*>(&transpose_w2_kernel), gt, dim3(256), xargs, 0, st) != cudaSuccess)
       return SPECV_ERR_CUDA;
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {cuuint64_t(rank), cuuint64_t(V)};
-    const cuuint64_t gstride[1] = {cuuint64_t(rank) * 2};
-    const cuuint32_t box[2] = {64, uint32_t(kTcBN)};
-    const cuuint32_t estride[2] = {1, 1};
-    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w2t, gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SPECV_ERR_CUDA;
+    // tensor maps: W2^T [V, rank]; U [R, gamma, V]; logits [R, slots, V] (slots = gamma, or 1 for the scratch row)
+    const long slots = draft_logits ? gamma : 1;
+    const bool lbf = a.logits_bf16 != 0;
+    CUtensorMap tmap_w2t, tmap_u, tmap_l;
+    {
+      const cuuint64_t gdim[2] = {cuuint64_t(rank), cuuint64_t(V)};
+      const cuuint64_t gstride[1] = {cuuint64_t(rank) * 2};
+      const cuuint32_t box[2] = {64, uint32_t(kTcBN)};
+      const cuuint32_t es[2] = {1, 1};
+      if (encode(&tmap_w2t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w2t, gdim, gstride, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SPECV_ERR_CUDA;
+    }
+    {
+      const cuuint64_t gdim[3] = {cuuint64_t(V), cuuint64_t(gamma), cuuint64_t(R)};
+      const cuuint64_t gstride[2] = {cuuint64_t(V) * 2, cuuint64_t(gamma) * V * 2};
+      const cuuint32_t box[3] = {uint32_t(kTcBN), 1, uint32_t(kTcBM)};
+      const cuuint32_t es[3] = {1, 1, 1};
+      if (encode(&tmap_u, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), gdim, gstride, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SPECV_ERR_CUDA;
+    }
+    {
+      const cuuint64_t esz = lbf ? 2 : 4;
+      const cuuint64_t gdim[3] = {cuuint64_t(V), cuuint64_t(slots), cuuint64_t(R)};
+      const cuuint64_t gstride[2] = {cuuint64_t(V) * esz, cuuint64_t(slots) * V * esz};
+      const cuuint32_t box[3] = {lbf ? 64u : 32u, 1, 32};
+      const cuuint32_t es[3] = {1, 1, 1};
+      if (encode(&tmap_l, lbf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.logits,
+                 gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SPECV_ERR_CUDA;
+    }
     if (cudaFuncSetAttribute(reinterpret_cast<void*>(&markov_tc_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kTcSmem)) != cudaSuccess)
       return SPECV_ERR_CUDA;
@@ -643,20 +771,21 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     a.ntile = (V + kTcBN - 1) / kTcBN;
     ta.nkc = rank / 64;
     ta.ntiles = a.ntile;
-    const int n_mp = (R + kTcMB * kTcBM - 1) / (kTcMB * kTcBM);
-    ta.per_mp = nsm / n_mp > 0 ? nsm / n_mp : 1;
-    const dim3 g1(unsigned(n_mp * ta.per_mp));
-    const dim3 g2(unsigned((R + 3) / 4));
+    const int n_mb = (R + kTcBM - 1) / kTcBM;
+    ta.per_mb = nsm / n_mb > 0 ? nsm / n_mb : 1;
+    const dim3 g1(unsigned(n_mb * ta.per_mb));
     for (int k = 1; k <= gamma; ++k) {
       a.k = k;
       a.step_off = draft_logits ? long(k - 1) * V : 0;
       ta.m = a;
-      void* targs[] = {&tmap, &ta};
+      ta.lz = draft_logits ? k - 1 : 0;
+      void* targs[] = {&tmap_w2t, &tmap_u, &tmap_l, &ta};
       if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_tc_kernel), g1, dim3(kTcThreads), targs, kTcSmem, st) !=
           cudaSuccess)
         return SPECV_ERR_CUDA;
       void* sargs[] = {&a};
-      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), g2, dim3(128), sargs, 0, st) != cudaSuccess)
+      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), dim3(unsigned(R)), dim3(kSampleThreads),
+                           sargs, 0, st) != cudaSuccess)
         return SPECV_ERR_CUDA;
     }
     return SPECV_OK;
@@ -664,7 +793,6 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
   a.tile_w = kMkBN;
   a.ntile = (V + kMkBN - 1) / kMkBN;
   const dim3 g1(unsigned(a.ntile), unsigned((R + kMkBM - 1) / kMkBM));
-  const dim3 g2(unsigned((R + 3) / 4));
   for (int k = 1; k <= gamma; ++k) {
     a.k = k;
     a.step_off = draft_logits ? long(k - 1) * V : 0;
@@ -672,7 +800,8 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_logits_kernel), g1, dim3(kMkThreads), args, 0, st) !=
         cudaSuccess)
       return SPECV_ERR_CUDA;
-    if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), g2, dim3(128), args, 0, st) != cudaSuccess)
+    if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), dim3(unsigned(R)), dim3(kSampleThreads), args,
+                         0, st) != cudaSuccess)
       return SPECV_ERR_CUDA;
   }
   return SPECV_OK;
