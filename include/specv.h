@@ -232,7 +232,16 @@ SPECV_API specv_status specv_verify_tree_greedy(const void* target_logits, specv
  *   draft_tokens [R, gamma] int32 out (x_1 .. x_gamma).
  *   draft_logits [R, gamma, V] out or NULL: the raw L_k (before temperature)
  *   in logits_out_dtype (SPECV_F32 or SPECV_BF16).
- *   1 <= rank <= SPECV_MAX_MARKOV_RANK, rank % 16 == 0.
+ *   1 <= rank <= SPECV_MAX_MARKOV_RANK, rank % 16 == 0; V <= 262144 (larger V
+ *   returns SPECV_ERR_UNSUPPORTED).
+ * Execution: when rank is a multiple of 64 and at most 256, V is a multiple of
+ *   8 and U, W1 and draft_logits are 16-byte aligned, the contraction runs on
+ *   the tensor cores (tcgen05, bf16 x bf16 -> float32) after W2 is transposed
+ *   into the workspace once per call; other shapes use a CUDA-core kernel.
+ *   Both accumulate the rank products in float32 (order unspecified).
+ * Errors: SPECV_ERR_INVALID_ARG for bad sizes, NULL or misaligned pointers or
+ *   a short workspace; a previous token outside [0, V) or a uniform outside
+ *   [0, 1) gives draft token -1 and SPECV_ERR_DEVICE_DATA in the error word.
  */
 SPECV_API size_t specv_markov_draft_workspace_size(int R, int gamma, int V, int rank);
 SPECV_API specv_status specv_markov_draft(const void* U, const void* W1, const void* W2,

@@ -187,12 +187,14 @@ __global__ void __launch_bounds__(kMkThreads) markov_logits_kernel(MarkovArgs a)
 // (prefix over tiles in index order), rescan its logits; T = 0 takes the argmax.
 constexpr int kSampleThreads = 256;
 constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kSampleMaxPer = 16;     // tiles per thread: at most 4096 tiles per row
 
 __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArgs a) {
   __shared__ float s_f[kSampleWarps];
   __shared__ int s_i[kSampleWarps];
   __shared__ int s_sel;
-  __shared__ float s_base, s_target, s_M;
+  __shared__ float s_base, s_target;
+  pdl_wait_primary();                      // the logits and partials of this step are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x;
   const int x_prev = prev_token(a, r);
@@ -219,29 +221,40 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
         a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad_in ? -1 : i;
         if (bad_in) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
       }
+      pdl_launch_dependents();
     }
     return;
   }
-  // row maximum of the tile maxima (already times c2)
+  // this thread's contiguous run of tiles, cached in registers; row maximum of
+  // the tile maxima (already times c2)
+  const int per = (a.ntile + kSampleThreads - 1) / kSampleThreads;     // <= kSampleMaxPer
+  const int t0 = threadIdx.x * per, t1 = min(a.ntile, t0 + per);
+  float pa[kSampleMaxPer], pb[kSampleMaxPer];
   float M = neg_inf();
-  for (int t = threadIdx.x; t < a.ntile; t += kSampleThreads) M = fmaxf(M, part[t].a);
+#pragma unroll
+  for (int j = 0; j < kSampleMaxPer; ++j) {
+    pa[j] = neg_inf();
+    pb[j] = 0.f;
+    if (t0 + j < t1) {
+      const MarkovPart p = part[t0 + j];
+      pa[j] = p.a;
+      pb[j] = p.b;
+      M = fmaxf(M, p.a);
+    }
+  }
   M = warp_max(M);
   if (lane == 0) s_f[warp] = M;
   __syncthreads();
-  if (warp == 0) {
-    float m = lane < kSampleWarps ? s_f[lane] : neg_inf();
-    m = warp_max(m);
-    if (lane == 0) s_M = m;
-  }
-  __syncthreads();
-  M = s_M;
-  // each thread: a contiguous run of tiles; block-wide inclusive scan of the masses
-  const int per = (a.ntile + kSampleThreads - 1) / kSampleThreads;
-  const int t0 = threadIdx.x * per, t1 = min(a.ntile, t0 + per);
+  M = neg_inf();
+#pragma unroll
+  for (int w = 0; w < kSampleWarps; ++w) M = fmaxf(M, s_f[w]);
+  __syncthreads();                                 // s_f is reused below
+  // block-wide inclusive scan of the tile masses
   float lsum = 0.f;
-  for (int t = t0; t < t1; ++t) {
-    const MarkovPart p = part[t];
-    lsum += p.b * ex2(p.a - M);
+#pragma unroll
+  for (int j = 0; j < kSampleMaxPer; ++j) {
+    pb[j] = pb[j] > 0.f ? pb[j] * ex2(pa[j] - M) : 0.f;     // tile mass relative to the row maximum
+    lsum += pb[j];
   }
   float incl = warp_inclusive_scan(lsum);
   if (lane == 31) s_f[warp] = incl;
@@ -283,22 +296,23 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     float run = incl - lsum;
     int sel = -1;
     float base = 0.f;
-    for (int t = t0; t < t1; ++t) {
-      const MarkovPart p = part[t];
-      const float m = p.b * ex2(p.a - M);
-      if (m > 0.f) {
-        sel = t;
+    bool done = false;
+#pragma unroll
+    for (int j = 0; j < kSampleMaxPer; ++j) {
+      const float m = pb[j];
+      if (!done && m > 0.f) {
+        sel = t0 + j;
         base = run;
-        if (run + m > target) break;
+        done = run + m > target;
       }
-      run += m;
+      if (!done) run += m;
     }
     s_sel = sel;
     s_base = base;
   }
   __syncthreads();
   const int sel = s_sel;
-  if (warp != 0) return;
+  if (warp != 0) return;                   // warp 0 triggers the next step once the token is written
   bool bad = bad_in || sel < 0;
   if (!bad) {
     // rescan the selected tile's columns in index order
@@ -342,6 +356,7 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad ? -1 : tok;
     if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -406,6 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
+  pdl_wait_primary();                      // the previous step's tokens (and W2^T) are complete
   if (warp < kTcEpiWarps) {
     // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
     for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
@@ -588,6 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tmem_dealloc(tmem, kTcTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+  pdl_launch_dependents();
 }
 
 // W2 [rank, V] -> W2^T [V, rank]: 64 x 64 tiles through shared memory, two
@@ -688,6 +705,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     return SPECV_ERR_INVALID_ARG;
   const MarkovLayout L = markov_layout(R, V, rank);
   if (workspace_bytes < L.total) return SPECV_ERR_INVALID_ARG;
+  if ((V + kTcBN - 1) / kTcBN > kSampleThreads * kSampleMaxPer) return SPECV_ERR_UNSUPPORTED;   // V > 262144
   specv_status s = check_device();
   if (s != SPECV_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -779,13 +797,26 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       a.step_off = draft_logits ? long(k - 1) * V : 0;
       ta.m = a;
       ta.lz = draft_logits ? k - 1 : 0;
+      // programmatic dependent launch: each grid is scheduled while its
+      // predecessor drains and waits (griddepcontrol.wait) for its results
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      at[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.stream = st;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
       void* targs[] = {&tmap_w2t, &tmap_u, &tmap_l, &ta};
-      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_tc_kernel), g1, dim3(kTcThreads), targs, kTcSmem, st) !=
-          cudaSuccess)
+      cfg.gridDim = g1;
+      cfg.blockDim = dim3(kTcThreads);
+      cfg.dynamicSmemBytes = kTcSmem;
+      if (cudaLaunchKernelExC(&cfg, reinterpret_cast<void*>(&markov_tc_kernel), targs) != cudaSuccess)
         return SPECV_ERR_CUDA;
       void* sargs[] = {&a};
-      if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_sample_kernel), dim3(unsigned(R)), dim3(kSampleThreads),
-                           sargs, 0, st) != cudaSuccess)
+      cfg.gridDim = dim3(unsigned(R));
+      cfg.blockDim = dim3(kSampleThreads);
+      cfg.dynamicSmemBytes = 0;
+      if (cudaLaunchKernelExC(&cfg, reinterpret_cast<void*>(&markov_sample_kernel), sargs) != cudaSuccess)
         return SPECV_ERR_CUDA;
     }
     return SPECV_OK;
