@@ -131,6 +131,25 @@ def _cpu_threads() -> int:
     return 1
 
 
+def rank_seed(rank: int) -> int:
+    """Seed of rank `rank`'s batch: ranks verify independent request batches."""
+    return 3 + 1000 * rank
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time (ms) when running under torch.distributed, else `ms`."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def oracle_positions_per_s(case, budget_s: float):
     """Run the oracle request by request until `budget_s` elapses; positions/s."""
     import oracle
@@ -204,7 +223,7 @@ def run_ours(args):
         dist.barrier()
     specv.load()
 
-    case = synth.chain_batched(seed=3 + 1000 * rank, R=R)
+    case = synth.chain_batched(seed=rank_seed(rank), R=R)
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     target = to_dev(case.target.raw.view(np.int16)).view(torch.bfloat16)
     draft = to_dev(case.draft.raw.view(np.int16)).view(torch.bfloat16)
@@ -252,12 +271,9 @@ def run_ours(args):
     clocks = sampler.stop()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.fmean(times)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
     positions = R * GAMMA                   # lengths = gamma for every request
-    value = world * positions / (ms_max * 1e-3)
+    value = whole_job_rate(positions, world, ms_max)
 
     # end-to-end through the public API with pinned host buffers
     e2e = None
@@ -280,14 +296,11 @@ def run_ours(args):
             e.record(stream)
             torch.cuda.synchronize()
             e_times.append(s.elapsed_time(e))
-        e_ms = statistics.fmean(e_times)
-        e_t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        if dist is not None:
-            dist.all_reduce(e_t, op=dist.ReduceOp.MAX)
+        e_max = max_over_ranks(statistics.fmean(e_times), dist, dev)
         h2d = sum(t.numel() * t.element_size() for t in (h_t, h_d, h_x, h_u))
         d2h = sum(t.numel() * t.element_size() for t in (A_h, y_h, c_h))
-        e2e = {"value": world * positions / (float(e_t.item()) * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": float(e_t.item())}
+        e2e = {"value": whole_job_rate(positions, world, e_max), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_max}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -850,6 +850,7 @@ __global__ void __launch_bounds__(kArgmaxWarps * 32) argmax_tiles_kernel(ArgmaxA
     ar.i = idx;
     a.out[size_t(item) * a.ntile_stride + tile] = ar;
   }
+  pdl_launch_dependents();
 }
 
 struct GreedyArgs {
@@ -866,45 +867,49 @@ struct GreedyArgs {
   int sample;
 };
 
-__global__ void __launch_bounds__(32) greedy_finish_kernel(GreedyArgs a) {
+// One CTA per request, one warp per position: g_k = argmax target row k (and
+// the draft argmax for c*), then warp 0 finds the first mismatch by ballot.
+constexpr int kGreedyThreads = 256;
+
+__global__ void __launch_bounds__(kGreedyThreads) greedy_finish_kernel(GreedyArgs a) {
+  constexpr int NW = kGreedyThreads / 32;
+  __shared__ int s_g[SPECV_MAX_GAMMA + 1], s_gd[SPECV_MAX_GAMMA];
+  pdl_wait_primary();                      // the argmax tile records are complete
   const int r = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gamma = a.gamma;
-  int ell = a.lengths ? a.lengths[r] : gamma;
-  bool bad = ell < 0 || ell > gamma;
-  if (bad) ell = 0;
-  // g_k and the draft argmax for k < ell: lane k keeps row k (gamma <= 32)
-  int my_g = -1, my_gd = -1;
-  for (int k = 0; k < ell; ++k) {
-    const int g = combine_argmax(a.targ + size_t(r * a.tpos + k) * a.ntile_stride, a.nwt);
-    if (lane == k) my_g = g;
-    if (a.darg) {
-      const int gd = combine_argmax(a.darg + size_t(r * gamma + k) * a.ntile_stride, a.nwt);
-      if (lane == k) my_gd = gd;
+  int ell = a.lengths ? __ldg(a.lengths + r) : gamma;
+  const bool bad_len = ell < 0 || ell > gamma;
+  if (bad_len) ell = 0;
+  const int kt = a.sample ? ell : ell - 1;             // target rows used: 0 .. kt
+  for (int k = warp; k <= gamma; k += NW) {
+    int g = -1, gd = -1;
+    if (!bad_len && k <= kt) g = combine_argmax(a.targ + size_t(r * a.tpos + k) * a.ntile_stride, a.nwt);
+    if (!bad_len && a.darg && k < ell) gd = combine_argmax(a.darg + size_t(r * gamma + k) * a.ntile_stride, a.nwt);
+    if (lane == 0) {
+      s_g[k] = g;
+      if (k < gamma) s_gd[k] = gd;
     }
   }
-  if (a.c_star) {
-    for (int k = lane; k < gamma; k += 32) {
-      float c = __int_as_float(0x7fc00000);
-      if (!bad && k < ell) c = (my_gd == my_g) ? 1.f : 0.f;
-      a.c_star[size_t(r) * gamma + k] = c;
-    }
-  }
-  if (!a.sample) return;
+  __syncthreads();
+  if (a.c_star)
+    for (int k = threadIdx.x; k < gamma; k += kGreedyThreads)
+      a.c_star[size_t(r) * gamma + k] =
+          (!bad_len && k < ell) ? ((s_gd[k] == s_g[k]) ? 1.f : 0.f) : __int_as_float(0x7fc00000);
+  if (!a.sample || warp != 0) return;
   bool mismatch = false, valid = true;
   if (lane < ell) {
-    const int x = a.tokens[size_t(r) * gamma + lane];
+    const int x = __ldg(a.tokens + size_t(r) * gamma + lane);
     valid = x >= 0 && x < a.V;
-    mismatch = x != my_g;
+    mismatch = x != s_g[lane];
   }
-  bad = bad || __any_sync(0xffffffffu, !valid);
+  const bool bad = bad_len || __any_sync(0xffffffffu, !valid);
   const unsigned mm = __ballot_sync(0xffffffffu, mismatch);
   const int A = mm ? __ffs(mm) - 1 : ell;
   // correction (A < l_r) or bonus (A = l_r) token: the target argmax of row A
-  const int tok = combine_argmax(a.targ + size_t(r * a.tpos + A) * a.ntile_stride, a.nwt);
   if (lane == 0) {
     a.accepted[r] = bad ? -1 : A;
-    a.out_token[r] = bad ? -1 : tok;
+    a.out_token[r] = bad ? -1 : s_g[A];
     if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
 }
@@ -1285,7 +1290,8 @@ static specv_status chain_greedy(const void* target, const void* draft, specv_dt
   ga.ntile_stride = L.ntile_stride;
   ga.sample = sample ? 1 : 0;
   void* gargs[] = {&ga};
-  if (cudaLaunchKernel(reinterpret_cast<void*>(&greedy_finish_kernel), dim3(R), dim3(32), gargs, 0, st) != cudaSuccess)
+  if (launch_dependent(reinterpret_cast<void*>(&greedy_finish_kernel), dim3(R), dim3(kGreedyThreads), gargs, st) !=
+      cudaSuccess)
     return SPECV_ERR_CUDA;
   return SPECV_OK;
 }

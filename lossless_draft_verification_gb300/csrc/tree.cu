@@ -20,7 +20,7 @@
 
 namespace specv {
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 1024;   // one warp per node, 32 nodes per round
 
 struct TreeArgs {
   const int32_t* parents;     // [R, N+1]
@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeArgs a) {
   __shared__ int s_par[SPECV_MAX_TREE_NODES];
   __shared__ int s_tok[SPECV_MAX_TREE_NODES];
   __shared__ int s_best;
+  pdl_wait_primary();                      // the argmax tile records are complete
   const int r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N1 = a.N1;
@@ -158,7 +159,7 @@ extern "C" specv_status specv_verify_tree_greedy(const void* target_logits, spec
   ta.nwt = p.nwt;
   ta.stride = p.stride;
   void* args[] = {&ta};
-  if (cudaLaunchKernel(reinterpret_cast<void*>(&tree_walk_kernel), dim3(R), dim3(kTreeThreads), args, 0, st) !=
+  if (launch_dependent(reinterpret_cast<void*>(&tree_walk_kernel), dim3(R), dim3(kTreeThreads), args, st) !=
       cudaSuccess)
     return SPECV_ERR_CUDA;
   return SPECV_OK;
