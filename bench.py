@@ -430,7 +430,7 @@ def run_workload(args):
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                 "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
     elif w == "markov":
-        Rm, Gm, Vm, rank = 512, 7, 129280, 256
+        Rm, Gm, Vm, rank = 512, args.positions or 7, 129280, 256
         m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
         U, W1, W2 = bf(m.U), bf(m.W1), bf(m.W2)
         anchor, u = td(m.anchor, np.int32), td(m.uniforms, np.float32)
@@ -445,7 +445,7 @@ def run_workload(args):
         algo = Gm * (Rm * Vm * 2 + rank * Vm * 2 + Rm * Vm * 4)
         flops = Gm * 2 * Rm * rank * Vm
         units, unit, metric = Rm * Gm, "tokens/s", "Markov-head drafting: draft tokens/sec"
-        desc = "DSpark Markov head: R=512, gamma=7, V=129280, rank 256, T=1, float32 logits out"
+        desc = f"DSpark Markov head: R=512, gamma={Gm}, V=129280, rank 256, T=1, float32 logits out"
         launches, kernel = 2 * Gm, "markov logits + sample (whole call)"
         ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -491,6 +491,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain", choices=["chain", "greedy", "tv", "tree", "markov", "schedule"])
+    ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     if args.requests != R:
         R = args.requests
