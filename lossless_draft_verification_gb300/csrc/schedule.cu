@@ -8,7 +8,10 @@
 // taken entries of each request form a prefix and l_r is their count.
 //
 // Parallel form: survival products (float64, left to right, one thread per
-// request), a bitonic sort of (a, index) pairs in shared memory, a block-wide
+// request), a bitonic sort of (a, index) pairs -- each thread holds EPT
+// consecutive pairs in registers; compare-exchange distances below one warp's
+// span run in registers and through warp shuffles, longer ones through shared
+// memory -- then a block-wide
 // int64 prefix sum of the fixed-point increments floor(a * 2^48) (exact, so
 // identical to any sequential order), Theta_n for every n at once, and a
 // block minimum over the first descent.
@@ -36,9 +39,20 @@ __device__ __forceinline__ bool pair_less(unsigned long long ka, int ia, unsigne
   return ka < kb || (ka == kb && ia < ib);
 }
 
+// compare-exchange of a register pair: afterwards (k0, i0) <= (k1, i1) if `up`, else >=
+__device__ __forceinline__ void cas(unsigned long long& k0, int& i0, unsigned long long& k1, int& i1, bool up) {
+  const bool swap = up ? pair_less(k1, i1, k0, i0) : pair_less(k0, i0, k1, i1);
+  if (swap) {
+    const unsigned long long tk = k0; k0 = k1; k1 = tk;
+    const int ti = i0; i0 = i1; i1 = ti;
+  }
+}
+
+template <int EPT>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
+  constexpr int N_ARR = kSchedThreads * EPT;     // sorted array length (padding sorts last)
   extern __shared__ __align__(16) unsigned char smem[];
-  const int n_pad = a.n_pad;
+  const int n_pad = N_ARR;
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);     // ~bits(a): ascending = a descending
   int* idx = reinterpret_cast<int*>(key + n_pad);
   long long* pre = reinterpret_cast<long long*>(idx + n_pad);                // inclusive prefix of aQ (sorted)
@@ -73,24 +87,79 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   }
   __syncthreads();
 
-  // bitonic sort of (key, idx), ascending
+  // bitonic sort of (key, idx), ascending; thread t owns elements [t*EPT, t*EPT + EPT)
+  unsigned long long rk[EPT];
+  int ri[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    rk[e] = key[tid * EPT + e];
+    ri[e] = idx[tid * EPT + e];
+  }
+  const int lane = tid & 31;
   for (int size = 2; size <= n_pad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n_pad / 2; i += kSchedThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long k0 = key[lo], k1 = key[hi];
-        const int i0 = idx[lo], i1 = idx[hi];
-        const bool swap = up ? pair_less(k1, i1, k0, i0) : pair_less(k0, i0, k1, i1);
-        if (swap) {
-          key[lo] = k1; key[hi] = k0;
-          idx[lo] = i1; idx[hi] = i0;
+    int stride = size >> 1;
+    if (stride >= 32 * EPT) {
+      // long distances through shared memory
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        key[tid * EPT + e] = rk[e];
+        idx[tid * EPT + e] = ri[e];
+      }
+      __syncthreads();
+      for (; stride >= 32 * EPT; stride >>= 1) {
+        for (int i = tid; i < n_pad / 2; i += kSchedThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          unsigned long long k0 = key[lo], k1 = key[hi];
+          int i0 = idx[lo], i1 = idx[hi];
+          cas(k0, i0, k1, i1, (lo & size) == 0);
+          key[lo] = k0; key[hi] = k1;
+          idx[lo] = i0; idx[hi] = i1;
         }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        rk[e] = key[tid * EPT + e];
+        ri[e] = idx[tid * EPT + e];
       }
       __syncthreads();
     }
+    // distances inside a warp's span: partner thread tid ^ (stride / EPT), same slot
+    for (; stride >= EPT; stride >>= 1) {
+      const int m = stride / EPT;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const int g = tid * EPT + e;
+        const unsigned long long pk = __shfl_xor_sync(0xffffffffu, rk[e], m);
+        const int pi = __shfl_xor_sync(0xffffffffu, ri[e], m);
+        const bool lower = (g & stride) == 0;
+        const bool up = (g & size) == 0;
+        // the lower element keeps the smaller pair when ascending
+        const bool partner_less = pair_less(pk, pi, rk[e], ri[e]);
+        const bool take = (lower == up) ? partner_less : !partner_less;
+        if (take) {
+          rk[e] = pk;
+          ri[e] = pi;
+        }
+      }
+    }
+    // distances inside a thread
+#pragma unroll
+    for (int st = EPT / 2; st >= 1; st >>= 1) {
+      if (st > stride) continue;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e)
+        if ((e & st) == 0) cas(rk[e], ri[e], rk[e + st], ri[e + st], ((tid * EPT + e) & size) == 0);
+    }
   }
+  (void)lane;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    key[tid * EPT + e] = rk[e];
+    idx[tid * EPT + e] = ri[e];
+  }
+  __syncthreads();
 
   // fixed-point increments and their inclusive prefix (contiguous chunk per thread)
   const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
@@ -103,7 +172,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     pre[i] = run;
   }
   // block exclusive scan of the per-thread totals
-  const int lane = tid & 31, warp = tid >> 5;
+  const int warp = tid >> 5;
   long long v = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -196,9 +265,13 @@ extern "C" specv_status specv_schedule(const float* conf, const double* sps, int
   sa.R = R;
   sa.gamma = gamma;
   sa.B_max = B_max;
-  sa.n_pad = pow2_at_least(R * gamma < 2 ? 2 : R * gamma);
+  const int n_pad = pow2_at_least(R * gamma < 2 ? 2 : R * gamma);
+  const int ept = n_pad <= 2 * kSchedThreads ? 2 : n_pad <= 4 * kSchedThreads ? 4 : 8;
+  sa.n_pad = ept * kSchedThreads;
   const size_t smem = sched_smem(R, sa.n_pad);
-  const void* fn = reinterpret_cast<const void*>(&schedule_kernel);
+  const void* fn = ept == 2 ? reinterpret_cast<const void*>(&schedule_kernel<2>)
+                 : ept == 4 ? reinterpret_cast<const void*>(&schedule_kernel<4>)
+                            : reinterpret_cast<const void*>(&schedule_kernel<8>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SPECV_ERR_CUDA;
   void* args[] = {&sa};
