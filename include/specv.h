@@ -235,9 +235,9 @@ SPECV_API specv_status specv_verify_tree_greedy(const void* target_logits, specv
  *   1 <= rank <= SPECV_MAX_MARKOV_RANK, rank % 16 == 0; V <= 262144 (larger V
  *   returns SPECV_ERR_UNSUPPORTED).
  * Execution: when rank is a multiple of 64 and at most 256, V is a multiple of
- *   8 and U, W1 and draft_logits are 16-byte aligned, the contraction runs on
- *   the tensor cores (tcgen05, bf16 x bf16 -> float32) after W2 is transposed
- *   into the workspace once per call; other shapes use a CUDA-core kernel.
+ *   8 and U, W1, W2 and draft_logits are 16-byte aligned, the contraction
+ *   runs on the tensor cores (tcgen05, bf16 x bf16 -> float32, W2 read in
+ *   place); other shapes use a CUDA-core kernel.
  *   Both accumulate the rank products in float32 (order unspecified).
  * Errors: SPECV_ERR_INVALID_ARG for bad sizes, NULL or misaligned pointers or
  *   a short workspace; a previous token outside [0, V) or a uniform outside

@@ -11,8 +11,8 @@
 //                   M = 128 blocks) and a strided set of 64-column vocabulary
 //                   tiles.  The W1[x_{k-1}] rows are gathered once into shared
 //                   memory (K-major, 128-byte swizzle); a TMA warp streams
-//                   tiles of W2^T (transposed once per call into the workspace)
-//                   through a two-stage ring; one thread issues tcgen05.mma
+//                   [rank x 64] tiles of W2 (read in place as an MN-major
+//                   operand) through a two-stage ring; one thread issues tcgen05.mma
 //                   (M = 128, N = 64, K = 16, bf16 -> float32) into a
 //                   double-buffered TMEM accumulator; eight epilogue warps read
 //                   TMEM, add U_k, write L and the tile's softmax partials.
@@ -369,12 +369,12 @@ constexpr int kTcThreads = (kTcEpiWarps + 2) * 32;   // + TMA warp + MMA warp
 constexpr uint32_t kTcTmemCols = 128;     // two accumulator buffers of 64 columns
 constexpr uint32_t kTcRowBytes = 128;     // one swizzled row
 constexpr size_t kTcSmemE = size_t(kTcMaxKC) * kTcBM * kTcRowBytes;        // 64 KB: W1 rows
-constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * kTcBN * kTcRowBytes;    // 64 KB: W2^T, two stages
+constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * 64 * kTcRowBytes;       // 64 KB: W2 tiles [rank][64], two stages
 constexpr size_t kTcSmemU = size_t(2) * kTcBM * kTcRowBytes;               // 32 KB: U tiles, two stages
 constexpr size_t kTcSmemL = size_t(kTcEpiWarps) * 2 * 32 * kTcRowBytes;    // 64 KB: logit staging per warp
 constexpr size_t kTcSmem = kTcSmemE + kTcSmemB + kTcSmemU + kTcSmemL + 1024;
 constexpr uint32_t kTcMaxPolls = 1u << 22;   // bound on every mbarrier wait
-constexpr uint32_t kTcIdesc = tc::idesc_bf16_f32(kTcBM, kTcBN);
+constexpr uint32_t kTcIdesc = tc::idesc_bf16_f32(kTcBM, kTcBN, true);   // B = W2, MN-major
 
 struct MarkovTcArgs {
   MarkovArgs m;
@@ -388,7 +388,7 @@ struct MarkovTcArgs {
 __device__ __forceinline__ uint32_t sw128(int r, int g) { return uint32_t(r) * kTcRowBytes + (uint32_t(g ^ (r & 7)) << 4); }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
-    markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2t, const __grid_constant__ CUtensorMap tmap_u,
+    markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
                      const __grid_constant__ CUtensorMap tmap_l, MarkovTcArgs ta) {
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int s_err;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
-  uint8_t* sB = sE + kTcSmemE;                      // [stage][rank chunk][64 rows][128 B]
+  uint8_t* sB = sE + kTcSmemE;                      // [stage][rank][128 B]: W2[k, n0 .. n0+64)
   uint8_t* sU = sB + kTcSmemB;                      // [stage][128 rows][128 B]  (64 bf16 per row)
   uint8_t* sL = sU + kTcSmemU;                      // [warp][2 halves][32 rows][128 B]  (32 floats per row)
 
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
-  pdl_wait_primary();                      // the previous step's tokens (and W2^T) are complete
+  pdl_wait_primary();                      // the previous step's tokens are complete
   if (warp < kTcEpiWarps) {
     // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
     for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
@@ -447,16 +447,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == kTcEpiWarps) {
-    // ---- TMA producer: W2^T rows [t*64, t*64+64) (MMA operand) and U_k[rows, t*64 .. +64) (epilogue)
+    // ---- TMA producer: W2[:, t*64 .. +64) (MMA operand) and U_k[rows, t*64 .. +64) (epilogue)
     if (lane == 0) {
       int i = 0;
       for (int t = j0; t < ta.ntiles; t += ta.per_mb, ++i) {
         const int s = i & 1;
         const uint32_t fresh = ((i >> 1) & 1) ^ 1;
         if (!mbar_wait_parity(&bar_empty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
-        mbar_arrive_expect_tx(&bar_full[s], uint32_t(ta.nkc) * kTcBN * kTcRowBytes);
-        for (int kc = 0; kc < ta.nkc; ++kc)
-          tc::tma_load_2d(sB + (size_t(s) * kTcMaxKC + kc) * (kTcBN * kTcRowBytes), &tmap_w2t, kc * 64, t * kTcBN,
+        mbar_arrive_expect_tx(&bar_full[s], uint32_t(ta.nkc) * 64 * kTcRowBytes);
+        for (int kc = 0; kc < ta.nkc; ++kc)     // 64 k-rows of 64 columns per box
+          tc::tma_load_2d(sB + (size_t(s) * kTcMaxKC + kc) * (64 * kTcRowBytes), &tmap_w2, t * kTcBN, kc * 64,
                           &bar_full[s]);
         if (!mbar_wait_parity(&bar_uempty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
         mbar_arrive_expect_tx(&bar_ufull[s], kTcBM * kTcRowBytes);
@@ -480,13 +480,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t aE = smem_addr(sE), aB = smem_addr(sB) + uint32_t(s) * kTcMaxKC * kTcBN * kTcRowBytes;
+        const uint32_t aE = smem_addr(sE), aB = smem_addr(sB) + uint32_t(s) * kTcMaxKC * 64 * kTcRowBytes;
         for (int kk = 0; kk < ta.nkc * 4; ++kk) {
           const uint64_t da = tc::smem_desc_k_sw128(aE + uint32_t(kk >> 2) * (kTcBM * kTcRowBytes) + uint32_t(kk & 3) * 32);
-          const uint64_t db = tc::smem_desc_k_sw128(aB + uint32_t(kk >> 2) * (kTcBN * kTcRowBytes) + uint32_t(kk & 3) * 32);
+          // 16 k-rows per instruction: two 1024-byte groups further along K
+          const uint64_t db = tc::smem_desc_mn_sw128(aB + uint32_t(kk) * 2048, 1024, 64 * 64 * 2);
           tc::mma_bf16(tmem + uint32_t(s * kTcBN), da, db, kTcIdesc, kk > 0 ? 1u : 0u);
         }
-        tc::commit(&bar_empty[s]);            // the W2^T stage is free once these MMAs have read it
+        tc::commit(&bar_empty[s]);            // the W2 stage is free once these MMAs have read it
         tc::commit(&bar_tfull[s]);            // the accumulator is ready for the epilogue
       }
       tc::commit(&bar_done);
@@ -607,46 +608,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
 }
 
-// W2 [rank, V] -> W2^T [V, rank]: 64 x 64 tiles through shared memory, two
-// bf16 per 32-bit access
-__global__ void __launch_bounds__(256) transpose_w2_kernel(const uint16_t* __restrict__ W2, uint16_t* __restrict__ W2T,
-                                                           int rank, int V) {
-  __shared__ uint16_t t[64][66];
-  const int v0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;    // 32 x 8
-  for (int i = ty; i < 64; i += 8) {
-    const int j = j0 + i, v = v0 + 2 * tx;
-    uint32_t w = 0;
-    if (j < rank && v + 1 < V) w = __ldg(reinterpret_cast<const uint32_t*>(W2 + size_t(j) * V + v));
-    else if (j < rank && v < V) w = W2[size_t(j) * V + v];
-    t[i][2 * tx] = uint16_t(w);
-    t[i][2 * tx + 1] = uint16_t(w >> 16);
-  }
-  __syncthreads();
-  for (int i = ty; i < 64; i += 8) {
-    const int v = v0 + i, j = j0 + 2 * tx;
-    if (v < V && j + 1 < rank)
-      *reinterpret_cast<uint32_t*>(W2T + size_t(v) * rank + j) = uint32_t(t[2 * tx][i]) | (uint32_t(t[2 * tx + 1][i]) << 16);
-    else if (v < V && j < rank)
-      W2T[size_t(v) * rank + j] = t[2 * tx][i];
-  }
-}
-
 namespace {
 // Workspace: header | tile partials [R, ceil(V / 64)] | float32 logits [R, V]
-// (when the caller keeps none) | W2^T [V, rank] bf16 (tensor-core form)
+// (when the caller keeps none)
 struct MarkovLayout {
-  size_t part_off, scratch_off, w2t_off, total;
+  size_t part_off, scratch_off, total;
 };
 MarkovLayout markov_layout(int R, int V, int rank) {
+  (void)rank;
   MarkovLayout L;
   size_t off = kHeaderBytes;
   L.part_off = off;
   off = align256(off + size_t(R) * ((V + kTcBN - 1) / kTcBN) * sizeof(MarkovPart));
   L.scratch_off = off;
   off = align256(off + size_t(R) * V * sizeof(float));
-  L.w2t_off = off;
-  if (rank % 64 == 0 && rank <= kTcMaxKC * 64 && V % 8 == 0) off = align256(off + size_t(V) * rank * 2);
   L.total = off;
   return L;
 }
@@ -735,27 +710,21 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
   a.greedy = temperature == 0.f;
   a.c2 = a.greedy ? 0.f : kLog2e / temperature;
   const bool tc_shape = rank % 64 == 0 && rank <= kTcMaxKC * 64 && V % 8 == 0 && aligned_to(U, 16) &&
-                        aligned_to(W1, 16) && (!draft_logits || aligned_to(draft_logits, 16));
+                        aligned_to(W1, 16) && aligned_to(W2, 16) && (!draft_logits || aligned_to(draft_logits, 16));
   PFN_cuTensorMapEncodeTiled_v12000 encode = tc_shape ? tensor_map_encoder() : nullptr;
   const int nsm = sm_count();
   if (encode != nullptr && nsm > 0) {
-    // tensor-core form: W2^T once, then per step the GEMM + epilogue and the sampler
-    uint16_t* w2t = reinterpret_cast<uint16_t*>(base + L.w2t_off);
-    const dim3 gt(unsigned((V + 63) / 64), unsigned((rank + 63) / 64));
-    const uint16_t* w2 = a.W2;
-    void* xargs[] = {&w2, &w2t, &rank, &V};
-    if (cudaLaunchKernel(reinterpret_cast<void*>(&transpose_w2_kernel), gt, dim3(256), xargs, 0, st) != cudaSuccess)
-      return SPECV_ERR_CUDA;
-    // tensor maps: W2^T [V, rank]; U [R, gamma, V]; logits [R, slots, V] (slots = gamma, or 1 for the scratch row)
+    // tensor-core form: per step the GEMM + epilogue and the sampler
+    // tensor maps: W2 [rank, V]; U [R, gamma, V]; logits [R, slots, V] (slots = gamma, or 1 for the scratch row)
     const long slots = draft_logits ? gamma : 1;
     const bool lbf = a.logits_bf16 != 0;
-    CUtensorMap tmap_w2t, tmap_u, tmap_l;
+    CUtensorMap tmap_w2, tmap_u, tmap_l;
     {
-      const cuuint64_t gdim[2] = {cuuint64_t(rank), cuuint64_t(V)};
-      const cuuint64_t gstride[1] = {cuuint64_t(rank) * 2};
-      const cuuint32_t box[2] = {64, uint32_t(kTcBN)};
+      const cuuint64_t gdim[2] = {cuuint64_t(V), cuuint64_t(rank)};
+      const cuuint64_t gstride[1] = {cuuint64_t(V) * 2};
+      const cuuint32_t box[2] = {uint32_t(kTcBN), 64};
       const cuuint32_t es[2] = {1, 1};
-      if (encode(&tmap_w2t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w2t, gdim, gstride, box, es,
+      if (encode(&tmap_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), gdim, gstride, box, es,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SPECV_ERR_CUDA;
@@ -806,7 +775,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       cfg.stream = st;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      void* targs[] = {&tmap_w2t, &tmap_u, &tmap_l, &ta};
+      void* targs[] = {&tmap_w2, &tmap_u, &tmap_l, &ta};
       cfg.gridDim = g1;
       cfg.blockDim = dim3(kTcThreads);
       cfg.dynamicSmemBytes = kTcSmem;

@@ -43,10 +43,25 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B (both K-major),
-// float32 accumulator, M x N tile.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// Shared-memory matrix descriptor for an MN-major operand in the canonical
+// 128-byte-swizzle layout: rows of 128 bytes hold 64 consecutive bf16 along
+// M or N for one k, groups of 8 k-rows are `k_group_bytes` apart, and blocks of
+// 64 along M or N are `mn_block_bytes` apart.  Group bases 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t k_group_bytes, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);           // start address
+  d |= uint64_t((mn_block_bytes >> 4) & 0x3FFFu) << 16;   // leading offset: next 64 along M or N
+  d |= uint64_t((k_group_bytes >> 4) & 0x3FFFu) << 32;    // stride offset: next 8 along K
+  d |= uint64_t(1) << 46;                          // descriptor version
+  d |= uint64_t(2) << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B, float32
+// accumulator, M x N tile; A K-major, B K-major or (b_mn_major) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one thread issues
