@@ -171,3 +171,21 @@ def test_batched_full_size(lib):
     print(f"\nbatched full size: {st.n} requests, {st.exact} exact, flagged accept {st.flagged_accept}, "
           f"flagged sample {st.flagged_sample}, mean accepted {A.mean():.2f} (oracle {res.accepted.mean():.2f})")
     assert st.exact >= st.n - 8
+
+
+def test_full_vocab_ragged_lengths(lib):
+    """V=151936 bf16 (the pipelined ten-slot tiling) with ragged l_r in [0, gamma]:
+    skipped positions, early bonus rows and l_r = 0 requests, T=1 and T=0."""
+    case = synth.chain_batched(seed=111, R=16, gamma=7, ragged_lengths=True)
+    assert (case.lengths == 0).any() or (case.lengths < 7).any()
+    st, A, y, res = _check_sampling(lib, case)
+    assert st.exact >= st.n - 2
+    g = synth.chain_batched(seed=112, R=12, gamma=7, temperature=0.0, ragged_lengths=True)
+    _check_greedy(lib, g)
+
+
+def test_max_gamma_full_vocab(lib):
+    """gamma = SPECV_MAX_GAMMA = 32 at V=151936 bf16: 33 positions per request."""
+    case = synth.chain_batched(seed=113, R=3, gamma=32)
+    st, A, y, res = _check_sampling(lib, case)
+    assert st.exact >= st.n - 1
