@@ -61,6 +61,19 @@ def test_tree_bad_parent_sets_error(lib):
     assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
 
 
+def test_tree_maximum_sizes(lib):
+    """1024 nodes (SPECV_MAX_TREE_NODES) and max_depth 64 (SPECV_MAX_TREE_DEPTH);
+    a 64-deep chain accepted to its end."""
+    case = synth.tree_greedy(seed=205, R=2, N=1023, max_depth=64, V=512, dtype="f32", p_follow=0.9)
+    _check_tree(lib, case)
+    chain = synth.tree_greedy(seed=206, R=2, N=64, max_depth=64, V=300, dtype="f32", p_follow=1.0)
+    chain.parents[:] = np.arange(-1, 64)
+    g = np.argmax(chain.target.f64, axis=-1)
+    chain.tokens[:, 1:] = g[:, :64]
+    ref = _check_tree(lib, chain)
+    assert (ref.path_len == 64).all()
+
+
 def test_tree_full_size(lib):
     """R=16 trees of 60 nodes + root, depth <= 8, V=151936 bf16."""
     case = synth.tree_greedy(seed=4)
