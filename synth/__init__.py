@@ -350,6 +350,17 @@ def markov(seed: int = 2, R: int = 1, gamma: int = 7, V: int = 151936, rank: int
     return MarkovCase(U, W1, W2, anchor, u, temperature)
 
 
+def dspark_target(seed: int, U: Logits) -> Logits:
+    """Target logits for verifying Markov drafts: rows k < gamma are U_k + sigma_r N(0,1)
+    with sigma_r ~ U(0.3, 2.0), the bonus row is N(0, 3^2); bf16 [R, gamma + 1, V]."""
+    R, gamma, V = U.raw.shape
+    sig = 0.3 + 1.7 * uniform_u24(seed, 41, (R, 1, 1))
+    t = np.empty((R, gamma + 1, V), dtype=np.float64)
+    t[:, :gamma] = U.f64 + sig * normal(seed, 42, (R, gamma, V))
+    t[:, gamma] = 3.0 * normal(seed, 43, (R, V))
+    return make_logits(t, "bf16")
+
+
 def confidences(seed: int = 5, R: int = 512, gamma: int = 7, mean: float = 1.5, sd: float = 1.0) -> np.ndarray:
     """c = sigmoid(N(mean, sd^2)) as float32 [R, gamma] (synthetic confidence-head output)."""
     z = mean + sd * normal(seed, 31, (R, gamma))

@@ -238,3 +238,37 @@ def test_schedule_bad_confidence(lib):
                               workspace=ws)
     assert (lengths.cpu().numpy() == -1).all()
     assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+
+
+# --------------------------------------------------------------------------- the DSpark round
+def test_dspark_round_full_size(lib):
+    """Markov drafting (R=512, gamma=7, V=129280, bf16 logits) -> scheduler -> chain
+    verification with the scheduled lengths, all on the device.  The scheduler's
+    lengths are checked bit-exact against the oracle (its inputs are synthetic);
+    the verification of GPU-made drafts is checked through properties that hold
+    for any input: 0 <= A_r <= l_r, tokens in [0, V), c* in [0, 1] for k < l_r and
+    NaN beyond."""
+    import torch
+    dev = torch.device("cuda")
+    R, G, V = 512, 7, 129280
+    m = synth.markov(seed=5, R=R, gamma=G, V=V)
+    tgt = synth.dspark_target(5, m.U)
+    U, W1, W2, target = (to_torch(x, dev) for x in (m.U, m.W1, m.W2, tgt))
+    toks, dlog = lib.markov_draft(U, W1, W2, to_torch(m.anchor, dev, np.int32), to_torch(m.uniforms, dev, np.float32),
+                                  1.0, True, torch.bfloat16)
+    conf = synth.confidences(5, R, G)
+    sps = synth.sps_table(4096)
+    lengths, _ = lib.schedule(to_torch(conf, dev, np.float32), to_torch(sps, dev, np.float64))
+    ell = lengths.cpu().numpy()
+    assert (ell == oracle.schedule(conf, sps).lengths).all()
+    u = to_torch(synth.uniform_f32(5, 44, (R, G + 1, 2)), dev, np.float32)
+    A, y, c = lib.verify_chain(target, dlog, toks, u, 1.0, lengths)
+    A, y, c = A.cpu().numpy(), y.cpu().numpy(), c.cpu().numpy()
+    t = toks.cpu().numpy()
+    assert ((t >= 0) & (t < V)).all()
+    assert ((A >= 0) & (A <= ell)).all() and ((y >= 0) & (y < V)).all()
+    k = np.arange(G)[None, :]
+    live = k < ell[:, None]
+    assert np.isnan(c[~live]).all()
+    assert ((c[live] >= -1e-6) & (c[live] <= 1 + 1e-6)).all()
+    print(f"\ndspark round: sum l_r {ell.sum()}, mean accepted {A.mean():.2f}, mean c* {c[live].mean():.3f}")
