@@ -39,6 +39,7 @@ constexpr int kStatsWarps = 8;        // warps (tiles) per CTA in chain_stats
 constexpr int kMaxCluster = 16;
 constexpr int kMaxTiles = kStatsWarps * kMaxCluster;   // 128 tiles per row
 constexpr int kFinishThreads = 256;
+constexpr int kMaxCompactRequests = 4096;   // ragged batches up to this R walk only their live items
 constexpr int kArgmaxWarps = 8;
 
 struct RowRec {
@@ -303,14 +304,14 @@ struct PipeArgs {
   int ncl;          // clusters in the grid
 };
 
-template <typename Elem, int VPT, int NW>
+template <typename Elem, int VPT, int NW, bool COMPACT>
 __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs pa) {
   using S = Slot<Elem, true>;
   constexpr int VW = S::VW;
   constexpr int kMaxParts = 8 * NW;             // cluster of at most 8 CTAs
   static_assert(kMaxParts <= 64, "two partials per lane");
   const StatsArgs& a = pa.s;
-  extern __shared__ uint4 s_stage[];            // [2 rows][VPT][threads]
+  extern __shared__ uint4 s_stage[];            // [2 rows][VPT][threads] (+ int[R + 1] when compacting)
   __shared__ float4 s_part[2][kMaxParts];       // every warp's partial of the cluster
 
   const uint32_t C = cluster_nctarank();
@@ -331,12 +332,63 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     jmax = n < VPT ? int(n) : VPT;
   }
 
-  // items of this cluster: item = cid + n * ncl, decoded incrementally into (r, k)
+  // Items of this cluster: o = cid, cid + ncl, ...  Without compaction item o is
+  // (o / P, o % P), decoded incrementally.  With ragged lengths (COMPACT) only
+  // the live items are walked: the CTA scans n_r = l_r (+1 for the bonus row;
+  // 0 for an invalid l_r) into s_pre and item o is (r, o - s_pre[r]) with
+  // s_pre[r] <= o < s_pre[r+1].
+  int n_items = pa.items;
+  [[maybe_unused]] int* s_pre = reinterpret_cast<int*>(s_stage + 2 * VPT * NW * 32);
+  if constexpr (COMPACT) {
+    const int R = pa.items / a.P;
+    const int per = (R + NW * 32 - 1) / (NW * 32);
+    const int r0 = threadIdx.x * per, r1 = min(R, r0 + per);
+    int cnt = 0;
+    for (int q = r0; q < r1; ++q) {
+      const int ell = __ldg(a.lengths + q);
+      cnt += (ell >= 0 && ell <= a.gamma) ? ell + a.with_bonus : 0;
+    }
+    __shared__ int s_wsum[NW];
+    const int lane_ = threadIdx.x & 31, warp_ = threadIdx.x >> 5;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane_ >= o) incl += t;
+    }
+    if (lane_ == 31) s_wsum[warp_] = incl;
+    __syncthreads();
+    int wpre = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      if (w < warp_) wpre += s_wsum[w];
+      total += s_wsum[w];
+    }
+    int run = wpre + incl - cnt;                 // live items before request r0
+    for (int q = r0; q < r1; ++q) {
+      s_pre[q] = run;
+      const int ell = __ldg(a.lengths + q);
+      run += (ell >= 0 && ell <= a.gamma) ? ell + a.with_bonus : 0;
+    }
+    if (threadIdx.x == 0) s_pre[R] = total;
+    __syncthreads();
+    n_items = total;
+  }
   const int dr = pa.ncl / a.P, dk = pa.ncl - (pa.ncl / a.P) * a.P;
-  auto advance = [&](int& r, int& k) {
+  auto advance = [&](int& r, int& k) {           // item + ncl, without compaction
     r += dr;
     k += dk;
     if (k >= a.P) { k -= a.P; ++r; }
+  };
+  auto locate = [&](int o, int& r, int& k) {     // item o, with compaction
+    int lo = 0, hi = pa.items / a.P;             // s_pre[lo] <= o < s_pre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= o) lo = mid;
+      else hi = mid;
+    }
+    r = lo;
+    k = o - s_pre[lo];
   };
   auto kind_of = [&](int r, int k) -> int {      // 0 skip, 1 row pair, 2 bonus row
     int ell = a.gamma;
@@ -359,7 +411,7 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     }
   };
   auto prefetch = [&](int item, int r, int k) {
-    if (item >= pa.items || jmax == 0) return;
+    if (item >= n_items || jmax == 0) return;
     const int kind = kind_of(r, k);
     if (kind == 0) return;
     copy_row(0, reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * size_t(V));
@@ -377,13 +429,29 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         *stage(1, j) = make_uint4(ninf, ninf, ninf, ninf);
       }
   }
-  int r = cid / a.P, k = cid - (cid / a.P) * a.P;        // current item
-  int rn = r, kn = k;                                    // next item
-  advance(rn, kn);
+  int r = 0, k = 0, rn = 0, kn = 0;                      // current and next item
+  if constexpr (COMPACT) {
+    if (cid < n_items) locate(cid, r, k);
+    if (cid + pa.ncl < n_items) locate(cid + pa.ncl, rn, kn);
+  } else {
+    r = cid / a.P;
+    k = cid - r * a.P;
+    rn = r;
+    kn = k;
+    advance(rn, kn);
+  }
+  auto step_next = [&](int o, int& r2, int& k2) {  // (r2, k2) becomes item o + ncl
+    if constexpr (COMPACT) {
+      if (o + pa.ncl < n_items) locate(o + pa.ncl, r2, k2);
+    } else {
+      advance(r2, k2);
+    }
+  };
   prefetch(cid, r, k);
   cp_async_commit();
   int processed = 0;
-  for (int item = cid; item < pa.items; item += pa.ncl, r = rn, k = kn, advance(rn, kn)) {
+  for (int o = cid; o < n_items; o += pa.ncl, r = rn, k = kn, step_next(o, rn, kn)) {
+    const int item = COMPACT ? r * a.P + k : o;   // storage index r * P + k
     const int kind = kind_of(r, k);
     cp_async_wait_all();                         // this thread's copies of `item` have landed
     // (the draft half of the stage is stale for a bonus row: its p results are dropped)
@@ -415,7 +483,7 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         mp = fmaxf(mp, tp[j].vmax());
       }
     }
-    prefetch(item + pa.ncl, rn, kn);
+    prefetch(o + pa.ncl, rn, kn);
     cp_async_commit();
     if (kind == 0) continue;
     if (kind == 2) mp = neg_inf();
@@ -1005,6 +1073,7 @@ struct KernelSet {
   void* stats;
   void* finish;
   void* argmax;
+  void* stats_compact;        // persistent form walking only the live items of ragged lengths
 };
 
 template <typename Elem, bool VEC>
@@ -1021,8 +1090,9 @@ KernelSet pick_vpt(int vpt) {
 
 template <typename Elem, int VPT>
 KernelSet pipe_set() {
-  return {reinterpret_cast<void*>(&chain_stats_pipe_kernel<Elem, VPT, kPipeWarps>),
-          reinterpret_cast<void*>(&chain_finish_kernel<Elem, true, VPT>), nullptr};
+  return {reinterpret_cast<void*>(&chain_stats_pipe_kernel<Elem, VPT, kPipeWarps, false>),
+          reinterpret_cast<void*>(&chain_finish_kernel<Elem, true, VPT>), nullptr,
+          reinterpret_cast<void*>(&chain_stats_pipe_kernel<Elem, VPT, kPipeWarps, true>)};
 }
 
 // clusters of the persistent kernel that fit at once, cached per device and kernel
@@ -1114,10 +1184,13 @@ specv_status launch_stats(const KernelSet& ks, const Tiling& t, const StatsArgs&
                           specv_dtype dtype) {
   if (items == 0) return SPECV_OK;
   if (t.pipe) {
-    const size_t smem = size_t(2) * t.vpt * t.warps * 32 * sizeof(uint4);
-    if (cudaFuncSetAttribute(ks.stats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    const int R = items / sa.P;
+    const bool compact = sa.lengths != nullptr && R <= kMaxCompactRequests;
+    void* fn = compact ? ks.stats_compact : ks.stats;
+    const size_t smem = size_t(2) * t.vpt * t.warps * 32 * sizeof(uint4) + (compact ? size_t(R + 1) * sizeof(int) : 0);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
       return SPECV_ERR_CUDA;
-    const int maxcl = max_active_clusters(ks.stats, smem, t.cluster, t.warps * 32);
+    const int maxcl = max_active_clusters(fn, smem, t.cluster, t.warps * 32);
     if (maxcl < 1) return SPECV_ERR_UNSUPPORTED;
     PipeArgs pa;
     pa.s = sa;
@@ -1136,7 +1209,7 @@ specv_status launch_stats(const KernelSet& ks, const Tiling& t, const StatsArgs&
     cfg.attrs = at;
     cfg.numAttrs = 1;
     void* args[] = {&pa};
-    if (cudaLaunchKernelExC(&cfg, ks.stats, args) != cudaSuccess) return SPECV_ERR_CUDA;
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SPECV_ERR_CUDA;
     return SPECV_OK;
   }
   cudaLaunchConfig_t cfg = {};
