@@ -464,18 +464,27 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
       tp[j].w[0] = u.x; tp[j].w[1] = u.y; tp[j].w[2] = u.z; tp[j].w[3] = u.w;
     }
     // tile maxima: consumes every staged value, so the slots are free to refill
+    // (the refill is issued between the cluster barrier's arrive and wait)
     float mq = neg_inf(), mp = neg_inf();
     if constexpr (sizeof(Elem) == 2) {
-      uint32_t aq = tq[0].w[0], ap = tp[0].w[0];
+      // pairwise (tree) reduction: a short dependency chain
+      auto max2 = [](uint32_t x, uint32_t y) {
+        uint32_t m;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(y));
+        return m;
+      };
+      auto slice_max = [&](const S* x) {
+        uint32_t m[VPT];
 #pragma unroll
-      for (int j = 0; j < VPT; ++j)
+        for (int j = 0; j < VPT; ++j) m[j] = max2(max2(x[j].w[0], x[j].w[1]), max2(x[j].w[2], x[j].w[3]));
 #pragma unroll
-        for (int i = (j == 0 ? 1 : 0); i < 4; ++i) {
-          asm("max.bf16x2 %0, %1, %2;" : "=r"(aq) : "r"(aq), "r"(tq[j].w[i]));
-          asm("max.bf16x2 %0, %1, %2;" : "=r"(ap) : "r"(ap), "r"(tp[j].w[i]));
-        }
-      mq = fmaxf(__uint_as_float(aq << 16), __uint_as_float(aq & 0xFFFF0000u));
-      mp = fmaxf(__uint_as_float(ap << 16), __uint_as_float(ap & 0xFFFF0000u));
+        for (int st = 1; st < VPT; st <<= 1)
+#pragma unroll
+          for (int j = 0; j + st < VPT; j += 2 * st) m[j] = max2(m[j], m[j + st]);
+        return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xFFFF0000u));
+      };
+      mq = slice_max(tq);
+      mp = slice_max(tp);
     } else {
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
@@ -483,15 +492,14 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         mp = fmaxf(mp, tp[j].vmax());
       }
     }
-    prefetch(o + pa.ncl, rn, kn);
-    cp_async_commit();
-    if (kind == 0) continue;
-    if (kind == 2) mp = neg_inf();
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
-      mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+    if (kind == 0) {
+      prefetch(o + pa.ncl, rn, kn);
+      cp_async_commit();
+      continue;
     }
+    if (kind == 2) mp = neg_inf();
+    mq = warp_max(mq);
+    mp = warp_max(mp);
     const bool q_live = mq > neg_inf();
     const bool p_live = mp > neg_inf();
     const float mq_c2 = q_live ? mq * c2 : 0.f;
@@ -528,17 +536,16 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
       if (lane < int(C)) st_shared_cluster_f4(cluster_map_shared(&s_part[pb][rank * NW + warp], uint32_t(lane)), part);
     }
     cluster_arrive_release();
+    // The next item's copies are issued only now: issued before the arrive,
+    // they held up its release fence.
+    prefetch(o + pa.ncl, rn, kn);
+    cp_async_commit();
     cluster_wait_acquire();
     const int nparts = int(C) * NW;
     const float4 none = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
     const float4 w0 = lane < nparts ? s_part[pb][lane] : none;
     const float4 w1 = lane + 32 < nparts ? s_part[pb][lane + 32] : none;
-    float Mq = fmaxf(w0.x, w1.x), Mp = fmaxf(w0.z, w1.z);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {             // every lane needs the row statistics
-      Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, o));
-      Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, o));
-    }
+    const float Mq = warp_max(fmaxf(w0.x, w1.x)), Mp = warp_max(fmaxf(w0.z, w1.z));
     float Zq = (w0.y > 0.f ? w0.y * ex2(w0.x - Mq) : 0.f) + (w1.y > 0.f ? w1.y * ex2(w1.x - Mq) : 0.f);
     float Zp = (w0.w > 0.f ? w0.w * ex2(w0.z - Mp) : 0.f) + (w1.w > 0.f ? w1.w * ex2(w1.z - Mp) : 0.f);
 #pragma unroll

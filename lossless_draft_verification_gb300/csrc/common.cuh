@@ -32,10 +32,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ float neg_inf() { return __uint_as_float(kF32NegInfBits); }
 
+// maximum over the warp in one instruction (exact; NaN inputs are ignored, as
+// by fmaxf)
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  float m;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
