@@ -165,8 +165,8 @@ SPECV_API specv_status specv_verify_chain(const void* target_logits, const void*
  * Errors: as specv_verify_chain; SPECV_ERR_INVALID_ARG also when
  *   specv_verify_chain_workspace_size(R, gamma, V, dtype) is 0, and
  *   SPECV_ERR_SCRATCH_LIMIT when it exceeds SPECV_NOALLOC_SCRATCH_BYTES
- *   (e.g. R = 1024, gamma = 7, V = 151936 bf16 needs about 15.6 MiB and fits;
- *   R = 2048 does not).  Both are decided on the host before any CUDA call.
+ *   (e.g. R = 1024, gamma = 7, V = 151936 bf16 needs about 8.1 MiB and fits;
+ *   R = 2048 needs 16.25 MiB and does not).  Both are decided on the host before any CUDA call.
  */
 SPECV_API specv_status specv_verify_chain_noalloc(const void* target_logits, const void* draft_logits,
                                        specv_dtype dtype, const int32_t* draft_tokens, const int32_t* lengths,

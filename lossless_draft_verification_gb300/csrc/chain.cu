@@ -1158,8 +1158,10 @@ KernelSet kernels_for(specv_dtype dtype, const Tiling& t) {
   return t.vec ? pick_vpt<float, true>(t.vpt) : pick_vpt<float, false>(t.vpt);
 }
 
-// Workspace: header | rows RowRec[items] | tiles TileStats[items][ntile_stride]
-//            | target argmax ArgRec[R*(gamma+1)][stride] | draft argmax ArgRec[R*gamma][stride]
+// Workspace: header | rows RowRec[items] | then either (T > 0) tiles
+// TileStats[items][ntile_stride], or (T = 0) target argmax
+// ArgRec[R*(gamma+1)][stride] | draft argmax ArgRec[R*gamma][stride].  A call
+// takes one of the two paths, so the two regions share their bytes.
 struct ChainLayout {
   size_t rows_off, tiles_off, targ_off, darg_off, total;
   int ntile_stride;
@@ -1173,12 +1175,11 @@ ChainLayout chain_layout(int R, int gamma, const Tiling& t) {
   L.rows_off = off;
   off = align256(off + items * sizeof(RowRec));
   L.tiles_off = off;
-  off = align256(off + items * L.ntile_stride * sizeof(TileStats));
   L.targ_off = off;
-  off = align256(off + items * L.ntile_stride * sizeof(ArgRec));
-  L.darg_off = off;
-  off = align256(off + size_t(R) * gamma * L.ntile_stride * sizeof(ArgRec));
-  L.total = off;
+  const size_t tiles_end = align256(off + items * L.ntile_stride * sizeof(TileStats));
+  L.darg_off = align256(off + items * L.ntile_stride * sizeof(ArgRec));
+  const size_t darg_end = align256(L.darg_off + size_t(R) * gamma * L.ntile_stride * sizeof(ArgRec));
+  L.total = tiles_end > darg_end ? tiles_end : darg_end;
   return L;
 }
 

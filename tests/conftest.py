@@ -1,6 +1,12 @@
 import os
 import sys
 
+# numpy asks the kernel for transparent huge pages on large arrays; where THP
+# defragmentation compacts memory on each fault, the oracle's large temporaries
+# then spend most of their time in the kernel.  Set before numpy is imported
+# (here and in the spawned workers, which inherit the environment).
+os.environ.setdefault("NUMPY_MADVISE_HUGEPAGE", "0")
+
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -22,3 +28,28 @@ def lib():
     build.build()
     specv.load()
     return specv
+
+
+@pytest.fixture(scope="session")
+def pool():
+    """Worker processes for the oracle's long Monte Carlo pins.  Their trials
+    are split into independent blocks of rows whose random numbers are the
+    same as in a single call, so spreading them over the host cores changes
+    no sample.  Spawned, never forked, so no parent state is inherited."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    n = max(1, min(8, os.cpu_count() or 1))
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"              # one thread per worker: no oversubscription
+    # glibc keeps freed blocks in the heap instead of unmapping them, so the
+    # oracle's repeated large temporaries reuse pages instead of faulting anew
+    os.environ["MALLOC_MMAP_MAX_"] = "0"
+    os.environ["MALLOC_TRIM_THRESHOLD_"] = str(1 << 34)
+    with ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn")) as ex:
+        yield ex
+
+
+def split_rows(n, parts):
+    """[start, stop) bounds of `parts` near-equal blocks of n rows."""
+    step = -(-n // parts)
+    return [(s, min(n, s + step)) for s in range(0, n, step)]

@@ -115,43 +115,56 @@ def _pair(kind, V):
     return q, p
 
 
+def _emitted_block(kind, V, m, seed):
+    """One block of the gamma = 1 trials: the first committed token of each."""
+    q0, p0 = _pair(kind, V)
+    q1 = _probs(16, 1, (V,))
+    q = np.broadcast_to(np.stack([q0, q1]), (m, 2, V))
+    p = np.broadcast_to(p0[None, None], (m, 1, V))
+    x = _draw(p, seed, 1)
+    u = synth.uniform_u24(seed, 2, (m, 2, 2))
+    res = oracle.verify_chain_probs(q, p, x, u)
+    emitted = np.where(res.accepted >= 1, x[:, 0], res.token)
+    return emitted, bool((res.accepted == 1).all()), bool((res.accepted == 0).all())
+
+
 @pytest.mark.parametrize("V", [8, 64])
 @pytest.mark.parametrize("kind", PAIRS)
-def test_first_emitted_token_is_distributed_as_q(V, kind):
+def test_first_emitted_token_is_distributed_as_q(V, kind, pool):
     """gamma = 1: the first committed token (x_0 if accepted, else the residual
     draw) must follow q exactly (DART notes §2.3 eq. (4))."""
     n = 1_000_000
-    q0, p0 = _pair(kind, V)
-    q1 = _probs(16, 1, (V,))
-    emitted = np.empty(n, dtype=np.int64)
+    q0, _ = _pair(kind, V)
     block = 200_000
-    for s in range(0, n, block):
-        m = min(block, n - s)
-        seed = 1000 + s // block
-        q = np.broadcast_to(np.stack([q0, q1]), (m, 2, V))
-        p = np.broadcast_to(p0[None, None], (m, 1, V))
-        x = _draw(p, seed, 1)
-        u = synth.uniform_u24(seed, 2, (m, 2, 2))
-        res = oracle.verify_chain_probs(q, p, x, u)
-        emitted[s:s + m] = np.where(res.accepted >= 1, x[:, 0], res.token)
-        if kind == "equal":
-            assert (res.accepted == 1).all()
-        if kind == "disjoint":
-            assert (res.accepted == 0).all()
+    futs = [pool.submit(_emitted_block, kind, V, min(block, n - s), 1000 + s // block) for s in range(0, n, block)]
+    parts = [f.result() for f in futs]
+    emitted = np.concatenate([e for e, _, _ in parts])
+    if kind == "equal":
+        assert all(all_acc for _, all_acc, _ in parts)
+    if kind == "disjoint":
+        assert all(all_rej for _, _, all_rej in parts)
     assert _chisq_ok(emitted, q0, V, n) > 1e-3
 
 
+def _bonus_block(q0, u):
+    m, V = u.shape[0], q0.shape[0]
+    q = np.broadcast_to(q0[None, None], (m, 1, V))
+    res = oracle.verify_chain_probs(q, np.zeros((m, 0, V)), np.zeros((m, 0), dtype=np.int64), u)
+    return res.accepted, res.token
+
+
 @pytest.mark.parametrize("V", [8, 64])
-def test_bonus_token_is_distributed_as_q(V):
+def test_bonus_token_is_distributed_as_q(V, pool):
+    from conftest import split_rows
     n = 1_000_000
     q0 = _probs(17, 1, (V,), 1.5)
-    q = np.broadcast_to(q0[None, None], (n, 1, V))
-    p = np.zeros((n, 0, V))
-    x = np.zeros((n, 0), dtype=np.int64)
     u = synth.uniform_u24(17, 2, (n, 1, 2))
-    res = oracle.verify_chain_probs(q, p, x, u)
-    assert (res.accepted == 0).all()
-    assert _chisq_ok(res.token, q0, V, n) > 1e-3
+    futs = [pool.submit(_bonus_block, q0, u[a:b]) for a, b in split_rows(n, 8)]
+    parts = [f.result() for f in futs]
+    accepted = np.concatenate([a for a, _ in parts])
+    token = np.concatenate([t for _, t in parts])
+    assert (accepted == 0).all()
+    assert _chisq_ok(token, q0, V, n) > 1e-3
 
 
 def test_disjoint_supports_residual_is_q():
@@ -205,33 +218,42 @@ def _expected_A_exact(qs, ps):
     return float((px[:, None] * surv).sum())
 
 
-def _expected_A_mc(qs, ps, n, seed):
+def _accepted_block(qs, ps, x, u):
+    m = x.shape[0]
     gamma, V = ps.shape
-    q = np.broadcast_to(np.concatenate([qs, qs[-1:]])[None], (n, gamma + 1, V))
+    q = np.broadcast_to(np.concatenate([qs, qs[-1:]])[None], (m, gamma + 1, V))
+    p = np.broadcast_to(ps[None], (m, gamma, V))
+    return oracle.verify_chain_probs(q, p, x, u).accepted
+
+
+def _expected_A_mc(qs, ps, n, seed, pool):
+    from conftest import split_rows
+    gamma, V = ps.shape
     p = np.broadcast_to(ps[None], (n, gamma, V))
     x = _draw(p, seed, 1)
     u = synth.uniform_u24(seed, 2, (n, gamma + 1, 2))
-    A = oracle.verify_chain_probs(q, p, x, u).accepted
+    futs = [pool.submit(_accepted_block, qs, ps, x[a:b], u[a:b]) for a, b in split_rows(n, 8)]
+    A = np.concatenate([f.result() for f in futs])
     return A.mean(), A.std() / np.sqrt(n)
 
 
-def test_expected_accept_length_eq2():
+def test_expected_accept_length_eq2(pool):
     gamma, V = 3, 3
     qs, ps = _position_pairs(18, gamma, V)
     c = oracle.tv_accept_probs(qs, ps)
     eq2 = float(np.cumprod(c).sum())            # sum_i prod_{j<=i} a_j with a_j = c*_j
     assert abs(_expected_A_exact(qs, ps) - eq2) < 1e-12
-    mean, se = _expected_A_mc(qs, ps, 1_000_000, 19)
+    mean, se = _expected_A_mc(qs, ps, 1_000_000, 19, pool)
     assert abs(mean - eq2) < 5 * se
 
 
-def test_expected_accept_length_constant_a_closed_form():
+def test_expected_accept_length_constant_a_closed_form(pool):
     gamma, V, a = 3, 3, 0.7
     qs, ps = _position_pairs(20, gamma, V, c_target=a)
     np.testing.assert_allclose(oracle.tv_accept_probs(qs, ps), a, atol=1e-12)
     closed = a * (1 - a ** gamma) / (1 - a)
     assert abs(_expected_A_exact(qs, ps) - closed) < 1e-12
-    mean, se = _expected_A_mc(qs, ps, 1_000_000, 21)
+    mean, se = _expected_A_mc(qs, ps, 1_000_000, 21, pool)
     assert abs(mean - closed) < 5 * se
 
 

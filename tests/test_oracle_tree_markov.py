@@ -141,7 +141,13 @@ def test_markov_matches_explicit_transition_matrix():
             prev = toks[:, k]
 
 
-def test_markov_pair_chi_square():
+def _markov_block(U, W1, W2, anchor, u):
+    m, V = u.shape[0], U.shape[-1]
+    toks, _, _, _ = oracle.markov_draft(np.broadcast_to(U[None], (m, 2, V)), W1, W2, np.full(m, anchor), u, 1.0)
+    return toks
+
+
+def test_markov_pair_chi_square(pool):
     """(x_1, x_2) sampled by the head follows p_1(x_1) p_2(x_2 | x_1) over V^2 cells."""
     V, rank, n = 8, 4, 1_000_000
     m = synth.markov(seed=43, R=1, gamma=2, V=V, rank=rank, w_scale=1.0, u_scale=1.0)
@@ -151,9 +157,10 @@ def test_markov_pair_chi_square():
     p1 = scipy.special.softmax(U[0] + B[anchor])
     p2 = scipy.special.softmax(U[1][None, :] + B, axis=-1)       # row = x_1
     expected = (p1[:, None] * p2).ravel()
-    Ub = np.broadcast_to(U[None], (n, 2, V))
+    from conftest import split_rows
     u = synth.uniform_u24(43, 50, (n, 2))
-    toks, _, _, _ = oracle.markov_draft(Ub, W1, W2, np.full(n, anchor), u, 1.0)
+    futs = [pool.submit(_markov_block, U, W1, W2, anchor, u[a:b]) for a, b in split_rows(n, 8)]
+    toks = np.concatenate([f.result() for f in futs])
     counts = np.bincount(toks[:, 0] * V + toks[:, 1], minlength=V * V)
     assert scipy.stats.chisquare(counts, n * expected).pvalue > 1e-3
 
