@@ -390,6 +390,19 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     r = lo;
     k = o - s_pre[lo];
   };
+  // Without compaction the walk visits (r, k') and processes position
+  // k = (k' + r) mod P of request r.  Cluster c sees k' = (c + j * ncl) mod P;
+  // when ncl shares a factor with P (36 clusters, P = 8) that is only a few
+  // residues, so some clusters would get every cheap bonus row and others none.
+  // Rotating each request's positions by r mixes them.
+  auto rotate = [&](int r_, int k_) -> int {
+    if constexpr (COMPACT) {
+      return k_;
+    } else {
+      const int t = k_ + r_ % a.P;
+      return t >= a.P ? t - a.P : t;
+    }
+  };
   auto kind_of = [&](int r, int k) -> int {      // 0 skip, 1 row pair, 2 bonus row
     int ell = a.gamma;
     if (a.lengths) {
@@ -410,8 +423,9 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
         if (j < jmax) cp_async16(stage(row, j), src + base + j * 32 * VW);
     }
   };
-  auto prefetch = [&](int item, int r, int k) {
+  auto prefetch = [&](int item, int r, int kw) {
     if (item >= n_items || jmax == 0) return;
+    const int k = rotate(r, kw);
     const int kind = kind_of(r, k);
     if (kind == 0) return;
     copy_row(0, reinterpret_cast<const Elem*>(a.target) + (size_t(r) * a.Pt + k) * size_t(V));
@@ -451,8 +465,9 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
   cp_async_commit();
   int processed = 0;
   for (int o = cid; o < n_items; o += pa.ncl, r = rn, k = kn, step_next(o, rn, kn)) {
-    const int item = COMPACT ? r * a.P + k : o;   // storage index r * P + k
-    const int kind = kind_of(r, k);
+    const int kr = rotate(r, k);
+    const int item = r * a.P + kr;                // storage index
+    const int kind = kind_of(r, kr);
     cp_async_wait_all();                         // this thread's copies of `item` have landed
     // (the draft half of the stage is stale for a bonus row: its p results are dropped)
     S tq[VPT], tp[VPT];

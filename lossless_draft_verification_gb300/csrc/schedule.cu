@@ -8,9 +8,8 @@
 // taken entries of each request form a prefix and l_r is their count.
 //
 // Parallel form: survival products (float64, left to right, one thread per
-// request), a bitonic sort of (a, index) pairs -- each thread holds EPT
-// consecutive pairs in registers; compare-exchange distances below one warp's
-// span run in registers and through warp shuffles, longer ones through shared
+// request), a merge sort of (a, index) pairs that starts from the requests'
+// own runs (already ordered) -- ceil(log2 R) merge-path levels in shared
 // memory -- then a block-wide
 // int64 prefix sum of the fixed-point increments floor(a * 2^48) (exact, so
 // identical to any sequential order), Theta_n for every n at once, and a
@@ -39,15 +38,6 @@ __device__ __forceinline__ bool pair_less(unsigned long long ka, int ia, unsigne
   return ka < kb || (ka == kb && ia < ib);
 }
 
-// compare-exchange of a register pair: afterwards (k0, i0) <= (k1, i1) if `up`, else >=
-__device__ __forceinline__ void cas(unsigned long long& k0, int& i0, unsigned long long& k1, int& i1, bool up) {
-  const bool swap = up ? pair_less(k1, i1, k0, i0) : pair_less(k0, i0, k1, i1);
-  if (swap) {
-    const unsigned long long tk = k0; k0 = k1; k1 = tk;
-    const int ti = i0; i0 = i1; i1 = ti;
-  }
-}
-
 template <int EPT>
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   constexpr int N_ARR = kSchedThreads * EPT;     // sorted array length (padding sorts last)
@@ -57,6 +47,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   int* idx = reinterpret_cast<int*>(key + n_pad);
   long long* pre = reinterpret_cast<long long*>(idx + n_pad);                // inclusive prefix of aQ (sorted)
   int* ell = reinterpret_cast<int*>(pre + n_pad);                           // [R]
+  int* idx2 = ell + a.R;                                                     // merge buffer of idx
   __shared__ long long s_warp[kSchedThreads / 32];
   __shared__ int s_first;
   __shared__ int s_bad;
@@ -87,79 +78,58 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   }
   __syncthreads();
 
-  // bitonic sort of (key, idx), ascending; thread t owns elements [t*EPT, t*EPT + EPT)
-  unsigned long long rk[EPT];
-  int ri[EPT];
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) {
-    rk[e] = key[tid * EPT + e];
-    ri[e] = idx[tid * EPT + e];
-  }
-  const int lane = tid & 31;
-  for (int size = 2; size <= n_pad; size <<= 1) {
-    int stride = size >> 1;
-    if (stride >= 32 * EPT) {
-      // long distances through shared memory
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        key[tid * EPT + e] = rk[e];
-        idx[tid * EPT + e] = ri[e];
+  // Sort (key, idx) ascending by merging runs.  A request's products do not
+  // increase with j (each factor is at most 1 and rounding is monotone), so
+  // [r*gamma, r*gamma + gamma) is already an ascending run, and the keys are
+  // distinct pairs (idx breaks ties): merging adjacent runs level by level
+  // gives the one sorted order.  Merge path: each thread writes EPT
+  // consecutive outputs, locating its first one (and the first one of a new
+  // block) by binary search over the two runs; the second buffer is the
+  // prefix array, unused until the sort is done.
+  {
+    unsigned long long* kin = key;
+    int* iin = idx;
+    unsigned long long* kout = reinterpret_cast<unsigned long long*>(pre);
+    int* iout = idx2;
+    for (int len = gamma; len > 0 && len < n; len <<= 1) {
+      const int p0 = tid * EPT;
+      int a0 = 0, la = 0, lb = 0, i = 0, j = 0, blk_end = -1;
+      for (int p = p0; p < p0 + EPT && p < n; ++p) {
+        if (p >= blk_end) {                      // first output of this thread or of a new block
+          const int b0 = (p / (2 * len)) * (2 * len);
+          a0 = b0;
+          la = min(len, n - b0);
+          lb = min(len, n - b0 - la);
+          blk_end = b0 + la + lb;
+          const int d = p - b0;
+          int lo = max(0, d - lb), hi = min(d, la);
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const int jb = a0 + la + d - 1 - mid;
+            if (pair_less(kin[a0 + mid], iin[a0 + mid], kin[jb], iin[jb])) lo = mid + 1;
+            else hi = mid;
+          }
+          i = lo;
+          j = d - lo;
+        }
+        const bool take_a = j >= lb || (i < la && pair_less(kin[a0 + i], iin[a0 + i], kin[a0 + la + j], iin[a0 + la + j]));
+        const int src = take_a ? a0 + i : a0 + la + j;
+        kout[p] = kin[src];
+        iout[p] = iin[src];
+        if (take_a) ++i; else ++j;
       }
       __syncthreads();
-      for (; stride >= 32 * EPT; stride >>= 1) {
-        for (int i = tid; i < n_pad / 2; i += kSchedThreads) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          unsigned long long k0 = key[lo], k1 = key[hi];
-          int i0 = idx[lo], i1 = idx[hi];
-          cas(k0, i0, k1, i1, (lo & size) == 0);
-          key[lo] = k0; key[hi] = k1;
-          idx[lo] = i0; idx[hi] = i1;
-        }
-        __syncthreads();
-      }
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        rk[e] = key[tid * EPT + e];
-        ri[e] = idx[tid * EPT + e];
+      unsigned long long* tk = kin; kin = kout; kout = tk;
+      int* ti = iin; iin = iout; iout = ti;
+    }
+    if (kin != key) {                            // the sorted order sits in the second buffer
+      for (int q = tid; q < n; q += kSchedThreads) {
+        key[q] = kin[q];
+        idx[q] = iin[q];
       }
       __syncthreads();
     }
-    // distances inside a warp's span: partner thread tid ^ (stride / EPT), same slot
-    for (; stride >= EPT; stride >>= 1) {
-      const int m = stride / EPT;
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        const int g = tid * EPT + e;
-        const unsigned long long pk = __shfl_xor_sync(0xffffffffu, rk[e], m);
-        const int pi = __shfl_xor_sync(0xffffffffu, ri[e], m);
-        const bool lower = (g & stride) == 0;
-        const bool up = (g & size) == 0;
-        // the lower element keeps the smaller pair when ascending
-        const bool partner_less = pair_less(pk, pi, rk[e], ri[e]);
-        const bool take = (lower == up) ? partner_less : !partner_less;
-        if (take) {
-          rk[e] = pk;
-          ri[e] = pi;
-        }
-      }
-    }
-    // distances inside a thread
-#pragma unroll
-    for (int st = EPT / 2; st >= 1; st >>= 1) {
-      if (st > stride) continue;
-#pragma unroll
-      for (int e = 0; e < EPT; ++e)
-        if ((e & st) == 0) cas(rk[e], ri[e], rk[e + st], ri[e + st], ((tid * EPT + e) & size) == 0);
-    }
   }
-  (void)lane;
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) {
-    key[tid * EPT + e] = rk[e];
-    idx[tid * EPT + e] = ri[e];
-  }
-  __syncthreads();
 
   // fixed-point increments and their inclusive prefix (contiguous chunk per thread)
   const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
@@ -172,7 +142,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     pre[i] = run;
   }
   // block exclusive scan of the per-thread totals
-  const int warp = tid >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
   long long v = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -230,7 +200,7 @@ int pow2_at_least(int n) {
   return p;
 }
 size_t sched_smem(int R, int n_pad) {
-  return size_t(n_pad) * (sizeof(unsigned long long) + sizeof(int) + sizeof(long long)) + size_t(R) * sizeof(int);
+  return size_t(n_pad) * (sizeof(unsigned long long) + 2 * sizeof(int) + sizeof(long long)) + size_t(R) * sizeof(int);
 }
 }  // namespace
 
