@@ -34,6 +34,19 @@ struct SchedArgs {
   int R, gamma, B_max, n_pad;
 };
 
+// floor(a * 2^48) for 0 <= a <= 1, from the bits of a in integer arithmetic.
+// a * 2^48 is exact in float64 (a power-of-two scaling), so this equals the
+// truncation of the float64 product.  (Values outside [0, 1] are flagged as
+// bad data before their result is used.)
+__device__ __forceinline__ long long fixed48(unsigned long long bits) {
+  const int e = int((bits >> 52) & 0x7FF);               // biased exponent
+  if (e == 0) return 0;                                  // zero or below 2^-1022
+  const unsigned long long m = (bits & 0xFFFFFFFFFFFFFull) | (1ull << 52);
+  const int sh = 1027 - e;                               // a * 2^48 = m * 2^(e - 1027)
+  if (sh >= 64 || sh <= 0) return 0;
+  return static_cast<long long>(m >> sh);
+}
+
 __device__ __forceinline__ bool pair_less(unsigned long long ka, int ia, unsigned long long kb, int ib) {
   return ka < kb || (ka == kb && ia < ib);
 }
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   long long run = 0;
   for (int i = b0; i < b0 + per && i < n_pad; ++i) {
     long long q = 0;
-    if (i < n) q = __double2ll_rz(__dmul_rn(__longlong_as_double(static_cast<long long>(~key[i])), kQuantum));
+    if (i < n) q = fixed48(~key[i]);
     run += q;
     pre[i] = run;
   }
@@ -171,13 +184,18 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     const long long tau = tau0 + (m > 0 ? pre[m - 1] : 0);
     return __dmul_rn(__ll2double_rn(tau), a.sps[R + m - 1]);
   };
+  // each Theta_m once, into the sorted keys' space (not needed any more)
+  double* th = reinterpret_cast<double*>(key);              // th[m - 1] = Theta_m
   for (int m = 1 + tid; m <= n; m += kSchedThreads) {
-    bool stop = R + m > a.B_max;
-    if (!stop) {
-      const double t = theta(m), tp = theta(m - 1);
-      stop = !(t > tp);
+    if (R + m <= a.B_max) {
+      th[m - 1] = theta(m);
       if (!(a.sps[R + m - 1] > 0.0)) s_bad = 1;
     }
+  }
+  __syncthreads();
+  const double theta0 = theta(0);
+  for (int m = 1 + tid; m <= n; m += kSchedThreads) {
+    const bool stop = R + m > a.B_max || !(th[m - 1] > (m > 1 ? th[m - 2] : theta0));
     if (stop) atomicMin(&s_first, m);
   }
   if (!(a.sps[R - 1] > 0.0) && tid == 0) s_bad = 1;
