@@ -12,6 +12,8 @@
  *   specv_markov_draft        the DSpark Markov draft head, sampled position by position
  *   specv_tv_accept           the analytic acceptance c* = 1 - 1/2 ||p_d - p_t||_1
  *   specv_schedule            DSpark's greedy throughput scheduler
+ *   specv_shard_*             host combines of per-shard partials for rows whose
+ *                             vocabulary is split over several GPUs
  *
  * Sources (cited per entry point below):
  *   [DART notes]   "DART：把草稿并行生成之后，还要补上哪些依赖？", DART reading
@@ -270,6 +272,58 @@ SPECV_API size_t specv_schedule_workspace_size(int R, int gamma);
 SPECV_API specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
                             int32_t* lengths, double* theta_best,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------ vocabulary-sharded combine
+ *
+ * Host functions (no device work, no CUDA call) for rows whose V logits are
+ * split over several GPUs in contiguous ascending slices, shard s holding
+ * token ids [off_s, off_s + V_s), off_0 = 0.  Each GPU reduces its own slice;
+ * the caller's communication layer gathers the per-shard partials (all
+ * arrays below are shard-major: element (s, r) at s * rows + r); these
+ * functions combine them identically on every rank.  Sums over shards
+ * (sum_v min(q, p), the residual mass sum_v [q - p]_+) need no function: they
+ * are plain all-reduce sums.  Arrays are caller-owned HOST memory.
+ *
+ * specv_shard_combine_normalisers -- softmax normaliser of a full row from
+ * per-shard (max, sum of exponentials) pairs [DART notes §2.3: q and p are
+ * softmaxes over the whole vocabulary].  Ex2 domain, as the kernels keep it:
+ *   part [shards, rows, 2] float32: (m_c2, Z) = (max_v x_v * c2,
+ *        sum_v 2^(x_v * c2 - m_c2)) over the shard's slice, c2 = log2(e)/T;
+ *        a shard with no element (or all -inf) gives Z = 0 (m_c2 ignored).
+ *   out  [rows, 2] float32: (M_c2, Z) with M_c2 = max over shards with Z > 0
+ *        and Z = sum_s Z_s * 2^(m_c2,s - M_c2) (accumulated in float64, shards
+ *        in ascending order); a row with no mass gives (-inf, 0).
+ *
+ * specv_shard_pick -- the shard an inverse-CDF draw over ascending token ids
+ * lands in [DART notes eq. (4) for the residual r = [q-p]_+/R; DSpark guide for
+ * the bonus draw from q]: the draw is y = min{v : C(v) > u * S}, C the
+ * cumulative weight and S the total.  With P_s the mass of the shards before s
+ * (float64, ascending s), the owning shard is the first s with
+ * P_s + mass_s > u * S, and that shard draws y from its own slice as
+ * min{v : C_s(v) > target}, C_s cumulative within the slice.
+ *   mass [shards, rows] float64 >= 0: each shard's total draw weight;
+ *   u [rows] float32 in [0, 1);
+ *   shard_out [rows] int32: the owning shard, or -1 when the row has no mass;
+ *   target_out [rows] float64: u * S - P_s (>= 0), the threshold inside it.
+ *   If rounding leaves no shard past u * S, the last shard with mass is taken
+ *   (the same rule as the in-shard draw's last positive weight).
+ *   A negative or non-finite mass, or u outside [0, 1), is SPECV_ERR_INVALID_ARG.
+ *
+ * specv_shard_argmax_combine -- greedy argmax of a full row from per-shard
+ * (max value, token id) pairs [SD survey §1.3]: the larger value wins, equal
+ * values go to the lower token id (the same tie rule as within a shard).
+ *   val [shards, rows] float32, idx [shards, rows] int32 (global token ids);
+ *   a shard with no element gives val = -inf, idx = INT32_MAX.
+ *   out [rows] int32: the row's argmax, or -1 if every shard was empty.
+ *
+ * All three return SPECV_ERR_INVALID_ARG for shards < 1, rows < 0 or a NULL
+ * array when rows > 0; otherwise SPECV_OK.
+ */
+SPECV_API specv_status specv_shard_combine_normalisers(const float* part, int shards, int rows, float* out);
+SPECV_API specv_status specv_shard_pick(const double* mass, int shards, int rows, const float* u,
+                                        int32_t* shard_out, double* target_out);
+SPECV_API specv_status specv_shard_argmax_combine(const float* val, const int32_t* idx, int shards, int rows,
+                                                  int32_t* out);
 
 /* ------------------------------------------------------------------ utilities */
 

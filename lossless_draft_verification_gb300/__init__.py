@@ -26,7 +26,8 @@ __all__ = [
     "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_verify_chain_noalloc", "specv_tv_accept_workspace_size", "specv_tv_accept",
     "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
     "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_read_device_error",
-    "specv_status_string", "specv_abi_version",
+    "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
+    "specv_shard_argmax_combine",
     "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "read_device_error",
 ]
 
@@ -58,6 +59,9 @@ EXPORTED = {
     "specv_read_device_error": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
     "specv_status_string": (ctypes.c_char_p, [_c_int]),
     "specv_abi_version": (_c_int, []),
+    "specv_shard_combine_normalisers": (_c_int, [_vp, _c_int, _c_int, _vp]),
+    "specv_shard_pick": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "specv_shard_argmax_combine": (_c_int, [_vp, _vp, _c_int, _c_int, _vp]),
 }
 
 _lib = None
@@ -160,6 +164,19 @@ def specv_status_string(status):
 
 def specv_abi_version():
     return _call("specv_abi_version")
+
+
+# host arrays (e.g. numpy ``.ctypes.data`` or CPU tensors' ``data_ptr()``)
+def specv_shard_combine_normalisers(part, shards, rows, out):
+    return _call("specv_shard_combine_normalisers", part, shards, rows, out)
+
+
+def specv_shard_pick(mass, shards, rows, u, shard_out, target_out):
+    return _call("specv_shard_pick", mass, shards, rows, u, shard_out, target_out)
+
+
+def specv_shard_argmax_combine(val, idx, shards, rows, out):
+    return _call("specv_shard_argmax_combine", val, idx, shards, rows, out)
 
 
 # --------------------------------------------------------------------------- tensor helpers
