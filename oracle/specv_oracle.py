@@ -45,6 +45,9 @@ Readings where the pages are silent (each one is listed in the design doc):
       Theta_n = float(tau_n) * SPS(B_n) in float64.
   R7  c* at T = 0 is the T -> 0+ limit: 1 if the draft and target argmaxes
       agree, else 0.
+  R13 the asynchronous scheduler's global search takes, among equal Theta_n,
+      the smallest n (verifying fewer tokens for the same throughput), and
+      counts n = 0 (bonus positions only) as a candidate.
 """
 from __future__ import annotations
 
@@ -56,7 +59,8 @@ import numpy as np
 __all__ = [
     "softmax_t", "inverse_cdf", "residual", "ChainResult", "verify_chain_probs", "verify_chain",
     "verify_chain_greedy", "tv_accept", "tv_accept_probs", "TreeResult", "verify_tree_greedy",
-    "markov_step", "markov_draft", "ScheduleResult", "schedule", "survival_products",
+    "markov_step", "markov_draft", "ScheduleResult", "schedule", "survival_products", "schedule_global",
+    "prune_threshold",
 ]
 
 
@@ -425,3 +429,66 @@ def schedule(conf: np.ndarray, sps: np.ndarray, B_max: int | None = None) -> Sch
         ell[r] += 1
         n += 1
     return ScheduleResult(ell, theta_best / Q, n)
+
+
+def schedule_global(conf: np.ndarray, sps: np.ndarray, B_max: int | None = None,
+                    conf_stale: np.ndarray | None = None) -> ScheduleResult:
+    """The asynchronous form of the scheduler (DSpark guide, production
+    deployment): the early stop is removed and the number of pool entries K is
+    the one that maximises Theta_n = tau_n * SPS(R + n) over every
+    n = 0 .. min(R * gamma, B_max - R), searched globally; on equal Theta the
+    smallest n (reading R13).  K is computed from `conf_stale`, confidence-head
+    outputs two steps old (default: `conf`), which keeps the truncation
+    independent of the tokens being verified; the entries verified are then the
+    top K of the pool ordered by the current survival products (dynamic top-K).
+    tau, the pool order and Theta_n are those of `schedule` (reading R6).
+    Returns the lengths from the current pool, Theta_K of the stale pool (in
+    token units) and K."""
+    conf = np.asarray(conf)
+    stale = conf if conf_stale is None else np.asarray(conf_stale)
+    sps = np.asarray(sps, dtype=np.float64)
+    R, gamma = conf.shape
+    if stale.shape != conf.shape:
+        raise ValueError("conf_stale must have the shape of conf")
+    if B_max is None:
+        B_max = len(sps)
+    if B_max < R or B_max > len(sps):
+        raise ValueError("need R <= B_max <= len(sps)")
+    Q = 1 << QUANTUM_BITS
+
+    def pool(c):
+        a = survival_products(c)
+        return sorted(((a[r, j], r, j) for r in range(R) for j in range(gamma)),
+                      key=lambda e: (-e[0], e[1], e[2]))
+
+    tau = R * Q
+    best_n, best_theta = 0, float(tau) * sps[R - 1]
+    for n, (a_rj, _, _) in enumerate(pool(stale), start=1):
+        if R + n > B_max:
+            break
+        tau += int(math.floor(a_rj * Q))
+        theta = float(tau) * sps[R + n - 1]
+        if theta > best_theta:
+            best_n, best_theta = n, theta
+    ell = np.zeros(R, dtype=np.int64)
+    for _, r, j in pool(conf)[:best_n]:
+        if j != ell[r]:
+            raise AssertionError("pool order broke prefix closure")
+        ell[r] += 1
+    return ScheduleResult(ell, best_theta / Q, best_n)
+
+
+def prune_threshold(conf: np.ndarray, threshold: float) -> np.ndarray:
+    """Confidence-threshold suffix pruning (SD survey §6.1): with the prefix
+    survival s_{r,i} = prod_{j<=i} c_{r,j} (float64, left to right), the draft of
+    request r is cut before its first position with s_{r,i} < threshold, so
+    l_r = #{i : s_{r,i} >= threshold} (s does not increase along i)."""
+    s = survival_products(conf)
+    keep = s >= float(threshold)
+    ell = np.zeros(s.shape[0], dtype=np.int64)
+    for r in range(s.shape[0]):
+        i = 0
+        while i < s.shape[1] and keep[r, i]:
+            i += 1
+        ell[r] = i
+    return ell

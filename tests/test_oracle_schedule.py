@@ -111,3 +111,102 @@ def test_fixed_point_reading_matches_real_arithmetic_on_random_cases():
             tau, B, best, n = tau + av, B + 1, th, n + 1
         assert n == res.n_included
         assert abs(best - res.theta_best) <= 1e-12 * best
+
+
+# --------------------------------------------------------------------------- asynchronous form
+def _brute_best(a, sps, B_max):
+    """max over every length vector of tau * SPS(B) (plain float64 sums), with
+    the smallest B among the maxima."""
+    R, gamma = a.shape
+    best = None
+    for ell in itertools.product(range(gamma + 1), repeat=R):
+        B = R + sum(ell)
+        if B > B_max:
+            continue
+        th = _theta(a, ell, sps)
+        if best is None or th > best[0] * (1 + 1e-12) or (abs(th - best[0]) <= 1e-12 * best[0] and B < best[1]):
+            best = (th, B)
+    return best
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_global_search_equals_brute_force_over_all_lengths(seed):
+    """With stale = current confidences the global search is the optimum over
+    every length vector: the top-n entries maximise tau for each batch size
+    because a_{r,j} does not increase with j (DSpark guide, scheduler)."""
+    rng = np.random.default_rng(900 + seed)
+    R, gamma = 3, 3
+    c = rng.uniform(0.05, 1.0, size=(R, gamma)).astype(np.float32)
+    sps = rng.uniform(0.2, 1.0, size=R * gamma + R).astype(np.float64)     # arbitrary, not unimodal
+    res = oracle.schedule_global(c, sps)
+    a = oracle.survival_products(c)
+    th, B = _brute_best(a, sps, len(sps))
+    assert res.theta_best == pytest.approx(th, rel=1e-12)
+    assert R + res.n_included == B
+    assert _theta(a, res.lengths, sps) == pytest.approx(th, rel=1e-12)
+
+
+def test_global_search_never_below_the_early_stop():
+    for seed in range(8):
+        c = synth.confidences(700 + seed, 16, 5)
+        sps = synth.sps_table(128)
+        g = oracle.schedule_global(c, sps)
+        e = oracle.schedule(c, sps)
+        assert g.theta_best >= e.theta_best
+        # the smooth decreasing table keeps Theta unimodal here: the two agree
+        assert (g.lengths == e.lengths).all()
+
+
+def test_saw_tooth_table_global_search_passes_the_cliff():
+    """SPS falls from 10 to 4 at B = 2 and then stays flat: the early stop halts
+    at n = 0 (Theta_1 = 1.9 * 4 < 10), the global search takes all three entries
+    (Theta_3 = (1 + 0.9 + 0.81 + 0.729) * 4 = 13.756)."""
+    c = np.array([[0.9, 0.9, 0.9]], dtype=np.float64)
+    sps = np.array([10.0, 4.0, 4.0, 4.0])
+    assert oracle.schedule(c, sps).lengths.tolist() == [0]
+    g = oracle.schedule_global(c, sps)
+    assert g.lengths.tolist() == [3] and g.n_included == 3
+    assert g.theta_best == pytest.approx(3.439 * 4.0, rel=1e-12)
+
+
+def test_stale_confidences_set_K_current_ones_pick_the_entries():
+    """K = 1 from the stale pool (Theta: 2 * 1 = 2, 2.9 * 0.8 = 2.32, 3.0 * 0.7 = 2.1);
+    the one entry taken is the current pool's top, request 1."""
+    stale = np.array([[0.9], [0.1]])
+    cur = np.array([[0.1], [0.9]])
+    sps = np.array([5.0, 1.0, 0.8, 0.7])
+    g = oracle.schedule_global(cur, sps, conf_stale=stale)
+    assert g.n_included == 1
+    assert g.lengths.tolist() == [0, 1]
+    assert g.theta_best == pytest.approx(2.9 * 0.8, rel=1e-12)
+
+
+def test_global_ties_take_the_smallest_n_and_respect_the_cap():
+    c = np.array([[0.5, 0.0, 0.0]])
+    sps = np.full(8, 2.0)                      # Theta_1 = Theta_2 = Theta_3 = 3.0
+    g = oracle.schedule_global(c, sps)
+    assert g.n_included == 1 and g.lengths.tolist() == [1]
+    c = synth.confidences(55, 4, 3)
+    g = oracle.schedule_global(c, np.full(64, 1.0), B_max=5)     # R + n <= 5
+    assert g.n_included == 1 and g.lengths.sum() == 1
+
+
+# --------------------------------------------------------------------------- threshold pruning
+def test_prune_threshold_hand_cases():
+    c = np.array([[0.9, 0.9, 0.5, 1.0], [0.4, 1.0, 1.0, 1.0], [0.5, 1.0, 1.0, 0.5]])
+    # s = [0.9, 0.81, 0.405, 0.405], [0.4, 0.4, 0.4, 0.4], [0.5, 0.5, 0.5, 0.25]
+    assert oracle.prune_threshold(c, 0.5).tolist() == [2, 0, 3]     # s >= threshold is kept
+    assert oracle.prune_threshold(c, 0.0).tolist() == [4, 4, 4]
+    assert oracle.prune_threshold(c, 1.5).tolist() == [0, 0, 0]
+
+
+def test_prune_threshold_is_the_survival_count_and_monotone():
+    c = synth.confidences(56, 32, 7)
+    s = oracle.survival_products(c)
+    prev = None
+    for th in np.linspace(0.0, 1.0, 21):
+        ell = oracle.prune_threshold(c, th)
+        assert (ell == (s >= th).sum(axis=1)).all()   # s does not increase, so the kept set is a prefix
+        if prev is not None:
+            assert (ell <= prev).all()
+        prev = ell
