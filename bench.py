@@ -467,6 +467,28 @@ def run_workload(args):
         units, unit, metric = 1, "schedules/s", "greedy scheduler: schedules/sec (latency-bound)"
         desc, launches, kernel = "scheduler: R=512, gamma=7, SPS table 4096 entries", 1, "schedule"
         roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "traffic": None, "kernel": kernel}
+    elif w in ("schedule_global", "prune"):
+        Rs, Gs = 512, 7
+        conf = td(synth.confidences(5, Rs, Gs))
+        lengths = torch.empty(Rs, dtype=torch.int32, device=dev)
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        if w == "schedule_global":
+            stale = td(synth.confidences(6, Rs, Gs))
+            sps = td(synth.sps_table(4096))
+            theta = torch.empty(1, dtype=torch.float64, device=dev)
+            call = lambda: check(specv.specv_schedule_global(conf.data_ptr(), stale.data_ptr(), sps.data_ptr(), Rs, Gs,
+                                                             4096, lengths.data_ptr(), theta.data_ptr(), ws.data_ptr(),
+                                                             ws.numel(), sp), "specv_schedule_global")
+            units, unit, metric = 1, "schedules/s", "asynchronous global-search scheduler: schedules/sec (latency-bound)"
+            desc, kernel = "global-search scheduler: R=512, gamma=7, stale and current confidences, SPS table 4096", "schedule"
+        else:
+            call = lambda: check(specv.specv_prune_threshold(conf.data_ptr(), Rs, Gs, 0.5, lengths.data_ptr(),
+                                                             ws.data_ptr(), ws.numel(), sp), "specv_prune_threshold")
+            units, unit, metric = 1, "prunings/s", "confidence-threshold pruning: calls/sec (latency-bound)"
+            desc, kernel = "threshold pruning: R=512, gamma=7, threshold 0.5", "prune"
+        ms, clocks = _timed(call, None, args.steps, args.warmup, stream)
+        launches = 1
+        roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "traffic": None, "kernel": kernel}
     elif w == "dspark":
         Rm, Gm, Vm, rank = 512, 7, 129280, 256
         m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
@@ -517,7 +539,7 @@ def run_workload(args):
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "bf16", "data": "synthetic",
            "config": {"workload": desc, "l2": "flushed (2x L2 write) before every timed step"
-                      if w != "schedule" else "inputs are a few KB (L2-resident)"},
+                      if w not in ("schedule", "schedule_global", "prune") else "inputs are a few KB (L2-resident)"},
            "roofline": roof, "gpu_launches": None if launches is None else launches * args.steps, "clocks": clocks}
     print(json.dumps(out), flush=True)
     return 0
@@ -535,7 +557,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "dspark"])
+                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "dspark"])
     ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     if args.requests != R:

@@ -12,6 +12,8 @@
  *   specv_markov_draft        the DSpark Markov draft head, sampled position by position
  *   specv_tv_accept           the analytic acceptance c* = 1 - 1/2 ||p_d - p_t||_1
  *   specv_schedule            DSpark's greedy throughput scheduler
+ *   specv_schedule_global     its asynchronous global-search form (dynamic top-K)
+ *   specv_prune_threshold     confidence-threshold suffix pruning
  *   specv_shard_*             host combines of per-shard partials for rows whose
  *                             vocabulary is split over several GPUs
  *
@@ -272,6 +274,45 @@ SPECV_API size_t specv_schedule_workspace_size(int R, int gamma);
 SPECV_API specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
                             int32_t* lengths, double* theta_best,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* specv_schedule_global -- the scheduler's asynchronous form [DSpark guide,
+ * production deployment: the batch size of the next step must be known before
+ * the current step ends, so the truncation count K is computed from confidence
+ * outputs two steps old, which isolates the decision from the tokens being
+ * verified; with that causal barrier the early stop is removed and K comes
+ * from an unconstrained global search, while the entries taken are the top K
+ * of the pool ordered by the current cumulative confidences].
+ *   K = argmax over n = 0 .. min(R * gamma, B_max - R) of
+ *       Theta_n = tau_n * SPS(R + n), tau_n and Theta_n as in specv_schedule but
+ *       on the pool built from conf_stale; the smallest n among equal Theta_n
+ *       (n = 0, bonus positions only, is a candidate).
+ *   lengths: the per-request counts among the top K entries of the pool built
+ *       from conf (a_{r,j} descending, ties by (r, j)); theta_best = Theta_K of
+ *       the stale pool, in tokens x SPS.
+ *   conf, conf_stale [R, gamma] float32 in [0, 1]; conf_stale may be NULL or
+ *   equal to conf (K and the entries then come from one pool).  Other
+ *   arguments, the workspace (specv_schedule_workspace_size) and errors as for
+ *   specv_schedule; a bad value in either confidence array gives -1 lengths.
+ */
+SPECV_API specv_status specv_schedule_global(const float* conf, const float* conf_stale, const double* sps,
+                                             int R, int gamma, int B_max, int32_t* lengths, double* theta_best,
+                                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* specv_prune_threshold -- confidence-threshold suffix pruning [SD survey
+ * §6.1: the confidence head's prefix survival s_i = prod_{j<=i} a_j; the
+ * low-confidence suffix below a threshold is cut before verification, falling
+ * back to a shorter draft].
+ *   s_{r,i} = prod_{j<=i} conf[r, j] in float64, multiplied left to right;
+ *   lengths[r] = the number of leading positions with s_{r,i} >= threshold
+ *   (s does not increase, so the kept positions are a prefix).
+ *   conf [R, gamma] float32 in [0, 1]; lengths [R] int32 out; threshold finite
+ *   or +-inf (NaN is SPECV_ERR_INVALID_ARG).  Workspace: the
+ *   specv_schedule_workspace_size bytes (the error word).  A confidence outside
+ *   [0, 1] gives that request -1 and SPECV_ERR_DEVICE_DATA.
+ */
+SPECV_API specv_status specv_prune_threshold(const float* conf, int R, int gamma, double threshold,
+                                             int32_t* lengths, void* workspace, size_t workspace_bytes,
+                                             void* stream);
 
 /* ------------------------------------------------------ vocabulary-sharded combine
  *

@@ -27,6 +27,8 @@ constexpr double kQuantum = 281474976710656.0;   // 2^48
 
 struct SchedArgs {
   const float* conf;
+  const float* conf_stale;    // global mode: confidences that set K (null: conf)
+  int global;                 // 0: greedy with the early stop; 1: global search, dynamic top-K
   const double* sps;
   void* workspace;
   int32_t* lengths;
@@ -51,35 +53,19 @@ __device__ __forceinline__ bool pair_less(unsigned long long ka, int ia, unsigne
   return ka < kb || (ka == kb && ia < ib);
 }
 
+// The pool of (key, idx) sorted ascending (a descending, ties by index) for
+// one confidence array; key = ~bits(a_{r,j}), idx = r * gamma + j.  Run by
+// the whole block; ends with the sorted pool in key / idx.
 template <int EPT>
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
-  constexpr int N_ARR = kSchedThreads * EPT;     // sorted array length (padding sorts last)
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int n_pad = N_ARR;
-  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);     // ~bits(a): ascending = a descending
-  int* idx = reinterpret_cast<int*>(key + n_pad);
-  long long* pre = reinterpret_cast<long long*>(idx + n_pad);                // inclusive prefix of aQ (sorted)
-  int* ell = reinterpret_cast<int*>(pre + n_pad);                           // [R]
-  int* idx2 = ell + a.R;                                                     // merge buffer of idx
-  __shared__ long long s_warp[kSchedThreads / 32];
-  __shared__ int s_first;
-  __shared__ int s_bad;
-
+__device__ __forceinline__ void build_pool(const float* conf, int R, int gamma, int n, int n_pad,
+                                           unsigned long long* key, int* idx, long long* pre, int* idx2, int* s_bad) {
   const int tid = threadIdx.x;
-  const int R = a.R, gamma = a.gamma, n = R * gamma;
-  if (tid == 0) {
-    *reinterpret_cast<int*>(a.workspace) = 0;
-    s_first = n + 1;
-    s_bad = 0;
-  }
-  for (int i = tid; i < R; i += kSchedThreads) ell[i] = 0;
-
   // survival products, one request per thread
   for (int r = tid; r < R; r += kSchedThreads) {
     double prod = 1.0;
     for (int j = 0; j < gamma; ++j) {
-      const float c = a.conf[size_t(r) * gamma + j];
-      if (!(c >= 0.f && c <= 1.f)) s_bad = 1;
+      const float c = conf[size_t(r) * gamma + j];
+      if (!(c >= 0.f && c <= 1.f)) *s_bad = 1;
       prod = __dmul_rn(prod, double(c));
       key[r * gamma + j] = ~static_cast<unsigned long long>(__double_as_longlong(prod));
       idx[r * gamma + j] = r * gamma + j;
@@ -143,6 +129,34 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
       __syncthreads();
     }
   }
+}
+
+template <int EPT>
+__global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedArgs a) {
+  constexpr int N_ARR = kSchedThreads * EPT;     // sorted array length (padding sorts last)
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int n_pad = N_ARR;
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);     // ~bits(a): ascending = a descending
+  int* idx = reinterpret_cast<int*>(key + n_pad);
+  long long* pre = reinterpret_cast<long long*>(idx + n_pad);                // inclusive prefix of aQ (sorted)
+  int* ell = reinterpret_cast<int*>(pre + n_pad);                           // [R]
+  int* idx2 = ell + a.R;                                                     // merge buffer of idx
+  __shared__ long long s_warp[kSchedThreads / 32];
+  __shared__ int s_first;
+  __shared__ int s_bad;
+  __shared__ double s_bestv[kSchedThreads / 32];
+  __shared__ int s_bestm[kSchedThreads / 32];
+
+  const int tid = threadIdx.x;
+  const int R = a.R, gamma = a.gamma, n = R * gamma;
+  if (tid == 0) {
+    *reinterpret_cast<int*>(a.workspace) = 0;
+    s_first = n + 1;
+    s_bad = 0;
+  }
+  for (int i = tid; i < R; i += kSchedThreads) ell[i] = 0;
+
+  build_pool<EPT>(a.global && a.conf_stale ? a.conf_stale : a.conf, R, gamma, n, n_pad, key, idx, pre, idx2, &s_bad);
 
   // fixed-point increments and their inclusive prefix (contiguous chunk per thread)
   const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
@@ -194,21 +208,92 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   }
   __syncthreads();
   const double theta0 = theta(0);
-  for (int m = 1 + tid; m <= n; m += kSchedThreads) {
-    const bool stop = R + m > a.B_max || !(th[m - 1] > (m > 1 ? th[m - 2] : theta0));
-    if (stop) atomicMin(&s_first, m);
-  }
   if (!(a.sps[R - 1] > 0.0) && tid == 0) s_bad = 1;
-  __syncthreads();
-  const int taken = s_first - 1;
+  int taken = 0;
+  double theta_taken = 0.0;
+  if (!a.global) {
+    // early stop: the first m >= 1 whose Theta does not rise
+    for (int m = 1 + tid; m <= n; m += kSchedThreads) {
+      const bool stop = R + m > a.B_max || !(th[m - 1] > (m > 1 ? th[m - 2] : theta0));
+      if (stop) atomicMin(&s_first, m);
+    }
+    __syncthreads();
+    taken = s_first - 1;
+    theta_taken = theta(taken);
+  } else {
+    // global search: the m in [0, min(n, B_max - R)] with the largest Theta,
+    // the smallest such m on equal values
+    const int m_lim = min(n, a.B_max - R);
+    double bv = tid == 0 ? theta0 : -1.0;
+    int bm = tid == 0 ? 0 : 0x7fffffff;
+    for (int m = 1 + tid; m <= m_lim; m += kSchedThreads) {
+      const double t = th[m - 1];
+      if (t > bv || (t == bv && m < bm)) { bv = t; bm = m; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int om = __shfl_xor_sync(0xffffffffu, bm, o);
+      if (ov > bv || (ov == bv && om < bm)) { bv = ov; bm = om; }
+    }
+    if (lane == 0) {
+      s_bestv[warp] = bv;
+      s_bestm[warp] = bm;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kSchedThreads / 32; ++w)
+        if (s_bestv[w] > bv || (s_bestv[w] == bv && s_bestm[w] < bm)) { bv = s_bestv[w]; bm = s_bestm[w]; }
+      s_first = bm + 1;
+      s_bestv[0] = bv;
+    }
+    __syncthreads();
+    taken = s_first - 1;
+    theta_taken = s_bestv[0];
+    // the entries themselves: the top `taken` of the current pool
+    if (a.conf_stale) {
+      __syncthreads();
+      build_pool<EPT>(a.conf, R, gamma, n, n_pad, key, idx, pre, idx2, &s_bad);
+    }
+  }
   for (int i = tid; i < taken; i += kSchedThreads) atomicAdd(&ell[idx[i] / gamma], 1);
   __syncthreads();
   const bool bad = s_bad != 0;
   for (int r = tid; r < R; r += kSchedThreads) a.lengths[r] = bad ? -1 : ell[r];
   if (tid == 0) {
-    if (a.theta_best) a.theta_best[0] = bad ? __longlong_as_double(0x7ff8000000000000ll) : theta(taken) / kQuantum;
+    if (a.theta_best) a.theta_best[0] = bad ? __longlong_as_double(0x7ff8000000000000ll) : theta_taken / kQuantum;
     if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
+}
+
+// Confidence-threshold suffix pruning, one thread per request: the prefix
+// survival s_{r,i} = prod_{j<=i} c_{r,j} (float64, left to right) and
+// l_r = the number of leading positions with s_{r,i} >= threshold.
+struct PruneArgs {
+  const float* conf;
+  void* workspace;
+  int32_t* lengths;
+  double threshold;
+  int R, gamma;
+};
+
+__global__ void __launch_bounds__(256) prune_kernel(PruneArgs a) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
+  __syncthreads();
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= a.R) return;
+  double prod = 1.0;
+  int ell = 0;
+  bool alive = true, bad = false;
+  for (int j = 0; j < a.gamma; ++j) {
+    const float c = a.conf[size_t(r) * a.gamma + j];
+    if (!(c >= 0.f && c <= 1.f)) bad = true;
+    prod = __dmul_rn(prod, double(c));
+    alive = alive && prod >= a.threshold;
+    ell += alive ? 1 : 0;
+  }
+  a.lengths[r] = bad ? -1 : ell;
+  if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
 }
 
 namespace {
@@ -231,21 +316,23 @@ extern "C" size_t specv_schedule_workspace_size(int R, int gamma) {
   return kHeaderBytes;
 }
 
-extern "C" specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
-                                       int32_t* lengths, double* theta_best, void* workspace, size_t workspace_bytes,
-                                       void* stream) {
+static specv_status schedule_launch(const float* conf, const float* conf_stale, int global, const double* sps,
+                                    int R, int gamma, int B_max, int32_t* lengths, double* theta_best,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
   if (R < 0 || gamma < 0 || B_max < 1 || size_t(R) * gamma > SPECV_MAX_SCHED_ENTRIES || R > B_max)
     return SPECV_ERR_INVALID_ARG;
   if (R == 0) return SPECV_OK;
   if ((gamma > 0 && !conf) || !sps || !lengths || !workspace) return SPECV_ERR_INVALID_ARG;
-  if (!aligned_to(conf, 4) || !aligned_to(sps, 8) || !aligned_to(lengths, 4) || !aligned_to(theta_best, 8) ||
-      !aligned_to(workspace, 256))
+  if (!aligned_to(conf, 4) || !aligned_to(conf_stale, 4) || !aligned_to(sps, 8) || !aligned_to(lengths, 4) ||
+      !aligned_to(theta_best, 8) || !aligned_to(workspace, 256))
     return SPECV_ERR_INVALID_ARG;
   if (workspace_bytes < kHeaderBytes) return SPECV_ERR_INVALID_ARG;
   specv_status s = check_device();
   if (s != SPECV_OK) return s;
   SchedArgs sa;
   sa.conf = conf;
+  sa.conf_stale = (global && gamma > 0 && conf_stale != conf) ? conf_stale : nullptr;
+  sa.global = global;
   sa.sps = sps;
   sa.workspace = workspace;
   sa.lengths = lengths;
@@ -264,6 +351,44 @@ extern "C" specv_status specv_schedule(const float* conf, const double* sps, int
     return SPECV_ERR_CUDA;
   void* args[] = {&sa};
   if (cudaLaunchKernel(fn, dim3(1), dim3(kSchedThreads), args, smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  return SPECV_OK;
+}
+
+extern "C" specv_status specv_schedule(const float* conf, const double* sps, int R, int gamma, int B_max,
+                                       int32_t* lengths, double* theta_best, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  return schedule_launch(conf, nullptr, 0, sps, R, gamma, B_max, lengths, theta_best, workspace, workspace_bytes,
+                         stream);
+}
+
+extern "C" specv_status specv_schedule_global(const float* conf, const float* conf_stale, const double* sps, int R,
+                                              int gamma, int B_max, int32_t* lengths, double* theta_best,
+                                              void* workspace, size_t workspace_bytes, void* stream) {
+  return schedule_launch(conf, conf_stale, 1, sps, R, gamma, B_max, lengths, theta_best, workspace, workspace_bytes,
+                         stream);
+}
+
+extern "C" specv_status specv_prune_threshold(const float* conf, int R, int gamma, double threshold,
+                                              int32_t* lengths, void* workspace, size_t workspace_bytes,
+                                              void* stream) {
+  if (R < 0 || gamma < 0 || !(threshold == threshold)) return SPECV_ERR_INVALID_ARG;
+  if (R == 0) return SPECV_OK;
+  if ((gamma > 0 && !conf) || !lengths || !workspace) return SPECV_ERR_INVALID_ARG;
+  if (!aligned_to(conf, 4) || !aligned_to(lengths, 4) || !aligned_to(workspace, 256)) return SPECV_ERR_INVALID_ARG;
+  if (workspace_bytes < kHeaderBytes) return SPECV_ERR_INVALID_ARG;
+  specv_status s = check_device();
+  if (s != SPECV_OK) return s;
+  PruneArgs pa;
+  pa.conf = conf;
+  pa.workspace = workspace;
+  pa.lengths = lengths;
+  pa.threshold = threshold;
+  pa.R = R;
+  pa.gamma = gamma;
+  void* args[] = {&pa};
+  if (cudaLaunchKernel(reinterpret_cast<const void*>(&prune_kernel), dim3(unsigned((R + 255) / 256)), dim3(256), args,
+                       0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPECV_ERR_CUDA;
   return SPECV_OK;
 }

@@ -240,6 +240,78 @@ def test_schedule_bad_confidence(lib):
     assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
 
 
+def _run_global(lib, conf, sps, stale=None, B_max=None):
+    import torch
+    dev = torch.device("cuda")
+    R, gamma = conf.shape
+    c = to_torch(conf, dev, np.float32)
+    cs = to_torch(stale, dev, np.float32) if stale is not None else None
+    t = to_torch(sps, dev, np.float64)
+    ell = torch.empty(R, dtype=torch.int32, device=dev)
+    theta = torch.empty(1, dtype=torch.float64, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    st = lib.specv_schedule_global(c.data_ptr(), cs.data_ptr() if cs is not None else None, t.data_ptr(), R, gamma,
+                                   B_max or len(sps), ell.data_ptr(), theta.data_ptr(), ws.data_ptr(), 256,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    return ell.cpu().numpy(), float(theta.cpu().numpy()[0]), ws
+
+
+@pytest.mark.parametrize("R,gamma", [(1, 1), (3, 3), (40, 7), (512, 7), (1000, 8), (8192, 1)])
+def test_schedule_global_matches_oracle(lib, R, gamma):
+    conf = synth.confidences(420 + R, R, gamma)
+    stale = synth.confidences(430 + R, R, gamma)
+    rng = np.random.default_rng(R)
+    sps = synth.sps_table(max(4096, R * (gamma + 1))) * rng.uniform(0.9, 1.1, max(4096, R * (gamma + 1)))  # saw-tooth
+    for st in (None, stale):
+        ell, theta, _ = _run_global(lib, conf, sps, st)
+        ref = oracle.schedule_global(conf, sps, conf_stale=st)
+        assert (ell == ref.lengths).all()
+        assert theta == ref.theta_best
+
+
+def test_schedule_global_hand_cases(lib):
+    ell, theta, _ = _run_global(lib, np.array([[0.9, 0.9, 0.9]]), np.array([10.0, 4.0, 4.0, 4.0]))
+    assert list(ell) == [3]                                           # past the cliff
+    ell, _, _ = _run_global(lib, np.array([[0.1], [0.9]]), np.array([5.0, 1.0, 0.8, 0.7]),
+                            stale=np.array([[0.9], [0.1]]))
+    assert list(ell) == [0, 1]                                        # K from stale, entry from current
+    ell, _, _ = _run_global(lib, np.array([[0.5, 0.0, 0.0]]), np.full(8, 2.0))
+    assert list(ell) == [1]                                           # ties: the smallest n
+    c = synth.confidences(57, 4, 3)
+    ell, _, _ = _run_global(lib, c, np.full(64, 1.0), B_max=5)
+    assert ell.sum() == 1                                             # batch cap
+    c[2, 1] = -0.5
+    ell, _, ws = _run_global(lib, c, np.full(64, 1.0))
+    assert (ell == -1).all()
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+
+
+@pytest.mark.parametrize("R,gamma", [(1, 1), (64, 7), (5000, 8)])
+def test_prune_threshold_matches_oracle(lib, R, gamma):
+    import torch
+    dev = torch.device("cuda")
+    conf = synth.confidences(440 + R, R, gamma)
+    c = to_torch(conf, dev, np.float32)
+    ell = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    s = oracle.survival_products(conf)
+    for th in (0.0, 0.3, 0.5, float(s[0, 0]), 0.95, 2.0):              # s[0, 0] exactly: kept (s >= threshold)
+        st = lib.specv_prune_threshold(c.data_ptr(), R, gamma, th, ell.data_ptr(), ws.data_ptr(), 256,
+                                       torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        assert (ell.cpu().numpy() == oracle.prune_threshold(conf, th)).all()
+    bad = conf.copy()
+    bad[0, 0] = float("nan")
+    cb = to_torch(bad, dev, np.float32)
+    assert lib.specv_prune_threshold(cb.data_ptr(), R, gamma, 0.5, ell.data_ptr(), ws.data_ptr(), 256,
+                                     torch.cuda.current_stream().cuda_stream) == 0
+    got = ell.cpu().numpy()
+    assert got[0] == -1 and (got[1:] == oracle.prune_threshold(conf, 0.5)[1:]).all()
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+
+
 # --------------------------------------------------------------------------- the DSpark round
 def test_dspark_round_full_size(lib):
     """Markov drafting (R=512, gamma=7, V=129280, bf16 logits) -> scheduler -> chain
