@@ -48,6 +48,8 @@ Readings where the pages are silent (each one is listed in the design doc):
   R13 the asynchronous scheduler's global search takes, among equal Theta_n,
       the smallest n (verifying fewer tokens for the same throughput), and
       counts n = 0 (bonus positions only) as a candidate.
+  R14 the confidence head's linear projection is one weight vector w over the
+      concatenation [h_k; W1[x_{k-1}]] plus a scalar bias; x_0 is the anchor.
 """
 from __future__ import annotations
 
@@ -60,7 +62,7 @@ __all__ = [
     "softmax_t", "inverse_cdf", "residual", "ChainResult", "verify_chain_probs", "verify_chain",
     "verify_chain_greedy", "tv_accept", "tv_accept_probs", "TreeResult", "verify_tree_greedy",
     "markov_step", "markov_draft", "ScheduleResult", "schedule", "survival_products", "schedule_global",
-    "prune_threshold",
+    "prune_threshold", "confidence_head",
 ]
 
 
@@ -476,6 +478,24 @@ def schedule_global(conf: np.ndarray, sps: np.ndarray, B_max: int | None = None,
             raise AssertionError("pool order broke prefix closure")
         ell[r] += 1
     return ScheduleResult(ell, best_theta / Q, best_n)
+
+
+def confidence_head(h: np.ndarray, W1: np.ndarray, w: np.ndarray, b: float, anchor: np.ndarray,
+                    draft_tokens: np.ndarray) -> np.ndarray:
+    """DSpark's confidence head (DSpark guide, confidence head: a light linear
+    projection plus a sigmoid over the backbone hidden state h_k and the Markov
+    embedding W1[x_{k-1}], giving the conditional survival probability c_k):
+    c_{r,k} = 1 / (1 + exp(-(w[:H] . h[r,k] + w[H:] . W1[x_{r,k-1}] + b))) in float64,
+    with x_{r,0} = anchor[r] and x_{r,k-1} = draft_tokens[r, k-2] for k >= 2
+    (reading R14).  h [R, gamma, H], W1 [V, r], w [H + r]; returns [R, gamma]."""
+    h = np.asarray(h, np.float64)
+    W1 = np.asarray(W1, np.float64)
+    w = np.asarray(w, np.float64)
+    R, gamma, H = h.shape
+    prev = np.concatenate([np.asarray(anchor, np.int64)[:, None],
+                           np.asarray(draft_tokens, np.int64)[:, :gamma - 1]], axis=1)      # x_{k-1}
+    z = h @ w[:H] + W1[prev] @ w[H:] + float(b)
+    return 1.0 / (1.0 + np.exp(-z))
 
 
 def prune_threshold(conf: np.ndarray, threshold: float) -> np.ndarray:

@@ -210,3 +210,39 @@ def test_prune_threshold_is_the_survival_count_and_monotone():
         if prev is not None:
             assert (ell <= prev).all()
         prev = ell
+
+
+# --------------------------------------------------------------------------- confidence head
+def test_confidence_head_zero_weights_give_the_sigmoid_of_the_bias():
+    rng = np.random.default_rng(3)
+    h = rng.normal(size=(2, 3, 8))
+    W1 = rng.normal(size=(10, 4))
+    c = oracle.confidence_head(h, W1, np.zeros(12), 0.7, np.array([1, 2]), np.array([[3, 4, 5], [6, 7, 8]]))
+    np.testing.assert_allclose(c, 1.0 / (1.0 + np.exp(-0.7)), rtol=0, atol=0)
+
+
+def test_confidence_head_hand_case_and_the_previous_token():
+    """One-hot features: h_k = e_k, W1[v] = v * e_0 (rank 2), w = [1, 2, 3 | 0.5, 0],
+    b = -1: z_k = w_h[k] + 0.5 * x_{k-1} - 1 with x_0 the anchor."""
+    H, r = 3, 2
+    h = np.eye(3)[None]                               # [1, 3, 3]: h_k = e_k
+    W1 = np.zeros((10, r)); W1[:, 0] = np.arange(10)
+    w = np.array([1.0, 2.0, 3.0, 0.5, 0.0])
+    c = oracle.confidence_head(h, W1, w, -1.0, np.array([4]), np.array([[6, 2, 9]]))
+    z = np.array([1.0 + 0.5 * 4 - 1.0, 2.0 + 0.5 * 6 - 1.0, 3.0 + 0.5 * 2 - 1.0])     # the last draft token is unused
+    expect = [1.0 / (1.0 + np.exp(-x)) for x in z]
+    np.testing.assert_allclose(c[0], expect, rtol=1e-15)
+    assert 0.0 < c.min() and c.max() < 1.0
+
+
+def test_confidence_head_matches_scipy_expit_and_flips_with_the_sign():
+    import scipy.special
+    rng = np.random.default_rng(4)
+    R, gamma, H, r, V = 5, 4, 16, 8, 30
+    h, W1, w = rng.normal(size=(R, gamma, H)), rng.normal(size=(V, r)), rng.normal(size=H + r)
+    a, x = rng.integers(0, V, R), rng.integers(0, V, (R, gamma))
+    c = oracle.confidence_head(h, W1, w, 0.3, a, x)
+    prev = np.concatenate([a[:, None], x[:, :gamma - 1]], axis=1)
+    z = np.einsum("rkh,h->rk", h, w[:H]) + np.einsum("rki,i->rk", W1[prev], w[H:]) + 0.3
+    np.testing.assert_allclose(c, scipy.special.expit(z), rtol=1e-13)
+    np.testing.assert_allclose(oracle.confidence_head(h, W1, -w, -0.3, a, x), 1.0 - c, atol=1e-14)
