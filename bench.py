@@ -489,6 +489,24 @@ def run_workload(args):
         ms, clocks = _timed(call, None, args.steps, args.warmup, stream)
         launches = 1
         roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "traffic": None, "kernel": kernel}
+    elif w == "confidence":
+        Rc, Gc, Hc, Vc, rank = 512, 7, 4096, 129280, 256
+        hc = bf(synth.make_logits(synth.normal(7, 1, (Rc, Gc, Hc)), "bf16"))
+        W1c = bf(synth.make_logits(0.02 * synth.normal(7, 2, (Vc, rank)), "bf16"))
+        wc = td((synth.normal(7, 3, (Hc + rank,)) / np.sqrt(Hc + rank)).astype(np.float32))
+        anc = td((synth.uniform_u24(7, 4, (Rc,)) * Vc).astype(np.int32))
+        tokc = td((synth.uniform_u24(7, 5, (Rc, Gc)) * Vc).astype(np.int32))
+        confo = torch.empty(Rc, Gc, dtype=torch.float32, device=dev)
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        call = lambda: check(specv.specv_confidence_head(hc.data_ptr(), W1c.data_ptr(), wc.data_ptr(), 0.5, anc.data_ptr(),
+                                                         tokc.data_ptr(), Rc, Gc, Hc, Vc, rank, confo.data_ptr(),
+                                                         ws.data_ptr(), ws.numel(), sp), "specv_confidence_head")
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        algo = Rc * Gc * (Hc + rank) * 2 + (Hc + rank) * 4 + Rc * Gc * 4
+        units, unit, metric = Rc * Gc, "positions/s", "confidence head: draft positions scored/sec"
+        desc, launches, kernel = "confidence head: R=512, gamma=7, H=4096, rank 256, V=129280 bf16", 1, "confidence"
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
     elif w == "dspark":
         Rm, Gm, Vm, rank = 512, 7, 129280, 256
         m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
@@ -557,7 +575,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "dspark"])
+                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "confidence", "dspark"])
     ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     if args.requests != R:

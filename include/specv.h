@@ -14,6 +14,7 @@
  *   specv_schedule            DSpark's greedy throughput scheduler
  *   specv_schedule_global     its asynchronous global-search form (dynamic top-K)
  *   specv_prune_threshold     confidence-threshold suffix pruning
+ *   specv_confidence_head     DSpark's confidence head c_k over all draft positions
  *   specv_shard_*             host combines of per-shard partials for rows whose
  *                             vocabulary is split over several GPUs
  *
@@ -297,6 +298,27 @@ SPECV_API specv_status specv_schedule(const float* conf, const double* sps, int 
 SPECV_API specv_status specv_schedule_global(const float* conf, const float* conf_stale, const double* sps,
                                              int R, int gamma, int B_max, int32_t* lengths, double* theta_best,
                                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* specv_confidence_head -- DSpark's confidence head [DSpark guide, confidence
+ * head: for each draft position k a light linear projection plus a sigmoid over
+ * the backbone hidden state h_k and the Markov embedding W1[x_{k-1}] outputs
+ * c_k, the probability that position k passes verification given that all
+ * earlier positions did; the scheduler multiplies them into a_{r,j}].
+ *   c[r, k] = sigmoid(w[0:H] . h[r, k] + w[H:H+rank] . W1[x_{r,k-1}] + b),
+ *   x_{r,0} = anchor[r], x_{r,k-1} = draft_tokens[r, k-2] for k >= 2 (the last
+ *   draft token is not used).  Accumulated in float32.
+ *   h [R, gamma, H] bf16; W1 [V, rank] bf16 (the Markov head's table);
+ *   w [H + rank] float32; b finite; anchor [R], draft_tokens [R, gamma] int32;
+ *   conf [R, gamma] float32 out.  16-byte aligned rows with H and rank multiples
+ *   of 8 take the vector path; other shapes run element by element.
+ *   Workspace: specv_confidence_head_workspace_size bytes (the error word).
+ *   A token outside [0, V) gives NaN for that position and SPECV_ERR_DEVICE_DATA.
+ */
+SPECV_API size_t specv_confidence_head_workspace_size(int R, int gamma);
+SPECV_API specv_status specv_confidence_head(const void* h, const void* W1, const float* w, float b,
+                                             const int32_t* anchor, const int32_t* draft_tokens, int R, int gamma,
+                                             int H, int V, int rank, float* conf, void* workspace,
+                                             size_t workspace_bytes, void* stream);
 
 /* specv_prune_threshold -- confidence-threshold suffix pruning [SD survey
  * §6.1: the confidence head's prefix survival s_i = prod_{j<=i} a_j; the

@@ -26,6 +26,7 @@ __all__ = [
     "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_verify_chain_noalloc", "specv_tv_accept_workspace_size", "specv_tv_accept",
     "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
     "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_schedule_global", "specv_prune_threshold",
+    "specv_confidence_head_workspace_size", "specv_confidence_head",
     "specv_read_device_error",
     "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
     "specv_shard_argmax_combine",
@@ -59,6 +60,9 @@ EXPORTED = {
     "specv_schedule": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "specv_schedule_global": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "specv_prune_threshold": (_c_int, [_vp, _c_int, _c_int, _c_double, _vp, _vp, _c_size, _vp]),
+    "specv_confidence_head_workspace_size": (_c_size, [_c_int, _c_int]),
+    "specv_confidence_head": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                       _vp, _c_size, _vp]),
     "specv_read_device_error": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
     "specv_status_string": (ctypes.c_char_p, [_c_int]),
     "specv_abi_version": (_c_int, []),
@@ -165,6 +169,16 @@ def specv_schedule_global(conf, conf_stale, sps, R, gamma, B_max, lengths, theta
 
 def specv_prune_threshold(conf, R, gamma, threshold, lengths, workspace, workspace_bytes, stream):
     return _call("specv_prune_threshold", conf, R, gamma, threshold, lengths, workspace, workspace_bytes, stream)
+
+
+def specv_confidence_head_workspace_size(R, gamma):
+    return _call("specv_confidence_head_workspace_size", R, gamma)
+
+
+def specv_confidence_head(h, W1, w, b, anchor, draft_tokens, R, gamma, H, V, rank, conf, workspace, workspace_bytes,
+                          stream):
+    return _call("specv_confidence_head", h, W1, w, b, anchor, draft_tokens, R, gamma, H, V, rank, conf, workspace,
+                 workspace_bytes, stream)
 
 
 def specv_read_device_error(workspace, stream, status_out):

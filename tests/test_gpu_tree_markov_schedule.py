@@ -312,6 +312,59 @@ def test_prune_threshold_matches_oracle(lib, R, gamma):
     assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
 
 
+# --------------------------------------------------------------------------- confidence head
+def _conf_case(seed, R, gamma, H, V, rank):
+    h = synth.make_logits(synth.normal(seed, 1, (R, gamma, H)), "bf16")
+    W1 = synth.make_logits(0.5 * synth.normal(seed, 2, (V, rank)), "bf16")
+    w = (synth.normal(seed, 3, (H + rank,)) / np.sqrt(H + rank)).astype(np.float32)
+    anchor = (synth.uniform_u24(seed, 4, (R,)) * V).astype(np.int64)
+    toks = (synth.uniform_u24(seed, 5, (R, gamma)) * V).astype(np.int64)
+    return h, W1, w, anchor, toks
+
+
+def _run_conf(lib, h, W1, w, b, anchor, toks, R, gamma, H, V, rank):
+    import torch
+    dev = torch.device("cuda")
+    ht = torch.from_numpy(np.ascontiguousarray(h.raw.view(np.int16))).to(dev)
+    W1t = torch.from_numpy(np.ascontiguousarray(W1.raw.view(np.int16))).to(dev)
+    wt = to_torch(w, dev, np.float32)
+    at, tt = to_torch(anchor, dev, np.int32), to_torch(toks, dev, np.int32)
+    out = torch.empty(R, gamma, dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    st = lib.specv_confidence_head(ht.data_ptr(), W1t.data_ptr(), wt.data_ptr(), b, at.data_ptr(), tt.data_ptr(), R,
+                                   gamma, H, V, rank, out.data_ptr(), ws.data_ptr(), 256,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64), ws
+
+
+@pytest.mark.parametrize("R,gamma,H,V,rank", [(512, 7, 4096, 129280, 256), (3, 4, 100, 50, 12), (1, 1, 8, 9, 8)])
+def test_confidence_head_matches_oracle(lib, R, gamma, H, V, rank):
+    """float32 accumulation of H + rank exact products: |dz| <= (H + rank) 2^-24
+    sum |w_i x_i|, and the sigmoid's slope is at most 1/4."""
+    h, W1, w, anchor, toks = _conf_case(80 + H, R, gamma, H, V, rank)
+    c, _ = _run_conf(lib, h, W1, w, 0.5, anchor, toks, R, gamma, H, V, rank)
+    ref = oracle.confidence_head(h.f64, W1.f64, w, 0.5, anchor, toks)
+    prev = np.concatenate([anchor[:, None], toks[:, :gamma - 1]], axis=1)
+    mag = np.abs(h.f64) @ np.abs(w[:H].astype(np.float64)) + np.abs(W1.f64[prev]) @ np.abs(w[H:].astype(np.float64))
+    bound = 1e-6 + (H + rank) * 2.0 ** -24 * mag / 4
+    assert (np.abs(c - ref) <= bound).all()
+    assert (c > 0).all() and (c < 1).all()
+
+
+def test_confidence_head_bad_token(lib):
+    R, gamma, H, V, rank = 4, 3, 64, 20, 8
+    h, W1, w, anchor, toks = _conf_case(90, R, gamma, H, V, rank)
+    anchor[2] = V                       # out of range: position 0 of request 2
+    toks[1, 0] = -1                     # conditions position 1 of request 1
+    c, ws = _run_conf(lib, h, W1, w, 0.0, anchor, toks, R, gamma, H, V, rank)
+    assert np.isnan(c[2, 0]) and np.isnan(c[1, 1])
+    ok = ~np.isnan(c)
+    assert ok.sum() == R * gamma - 2
+    assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
+
+
 # --------------------------------------------------------------------------- the DSpark round
 def test_dspark_round_full_size(lib):
     """Markov drafting (R=512, gamma=7, V=129280, bf16 logits) -> scheduler -> chain
