@@ -38,19 +38,23 @@ struct ConfArgs {
 __device__ __forceinline__ float dot_bf16(const uint16_t* x, const float* w, int n, bool vec, int lane) {
   float acc = 0.f;
   if (vec) {
+    // unrolled, two accumulators: each lane keeps several 16-byte loads in flight
+    float acc2 = 0.f;
+#pragma unroll 8
     for (int i = lane * 8; i < n; i += 32 * 8) {
       const uint4 v = ldg_stream(x + i);
       const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + i));
       const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + i + 4));
       acc = fmaf(__uint_as_float(v.x << 16), w0.x, acc);
-      acc = fmaf(__uint_as_float(v.x & 0xFFFF0000u), w0.y, acc);
+      acc2 = fmaf(__uint_as_float(v.x & 0xFFFF0000u), w0.y, acc2);
       acc = fmaf(__uint_as_float(v.y << 16), w0.z, acc);
-      acc = fmaf(__uint_as_float(v.y & 0xFFFF0000u), w0.w, acc);
+      acc2 = fmaf(__uint_as_float(v.y & 0xFFFF0000u), w0.w, acc2);
       acc = fmaf(__uint_as_float(v.z << 16), w1.x, acc);
-      acc = fmaf(__uint_as_float(v.z & 0xFFFF0000u), w1.y, acc);
+      acc2 = fmaf(__uint_as_float(v.z & 0xFFFF0000u), w1.y, acc2);
       acc = fmaf(__uint_as_float(v.w << 16), w1.z, acc);
-      acc = fmaf(__uint_as_float(v.w & 0xFFFF0000u), w1.w, acc);
+      acc2 = fmaf(__uint_as_float(v.w & 0xFFFF0000u), w1.w, acc2);
     }
+    acc += acc2;
   } else {
     for (int i = lane; i < n; i += 32) acc = fmaf(__uint_as_float(uint32_t(__ldg(x + i)) << 16), __ldg(w + i), acc);
   }
