@@ -50,6 +50,13 @@ Readings where the pages are silent (each one is listed in the design doc):
       counts n = 0 (bonus positions only) as a candidate.
   R14 the confidence head's linear projection is one weight vector w over the
       concatenation [h_k; W1[x_{k-1}]] plus a scalar bias; x_0 is the anchor.
+  R15 DART's tree construction without the n-gram index uses g == 1 in eq. (10),
+      depth i = 1..d for the future offsets (the notes leave the numbering
+      open), eps = 1e-10, and generation order (path rank, then token rank) to
+      break equal scores.
+  R16 node selection: key = min(own score, parent's key); the theta largest keys,
+      then the smaller depth, then generation order; ancestor-closed by
+      construction (the notes ask for closure but give no rule).
 """
 from __future__ import annotations
 
@@ -62,7 +69,7 @@ __all__ = [
     "softmax_t", "inverse_cdf", "residual", "ChainResult", "verify_chain_probs", "verify_chain",
     "verify_chain_greedy", "tv_accept", "tv_accept_probs", "TreeResult", "verify_tree_greedy",
     "markov_step", "markov_draft", "ScheduleResult", "schedule", "survival_products", "schedule_global",
-    "prune_threshold", "confidence_head",
+    "prune_threshold", "confidence_head", "DartTree", "dart_tree",
 ]
 
 
@@ -496,6 +503,90 @@ def confidence_head(h: np.ndarray, W1: np.ndarray, w: np.ndarray, b: float, anch
                            np.asarray(draft_tokens, np.int64)[:, :gamma - 1]], axis=1)      # x_{k-1}
     z = h @ w[:H] + W1[prev] @ w[H:] + float(b)
     return 1.0 / (1.0 + np.exp(-z))
+
+
+@dataclass
+class DartTree:
+    parents: np.ndarray         # int64 [R, theta+1]; parents[:, 0] = -1; -1 padding past n_nodes
+    tokens: np.ndarray          # int64 [R, theta+1]; tokens[:, 0] = the root placeholder 0
+    n_nodes: np.ndarray         # int64 [R]: 1 + selected nodes
+    depth: np.ndarray           # int64 [R, theta+1]
+    key: np.ndarray             # float64 [R, theta+1]: selection key of each node (root: +inf)
+    n_expanded: np.ndarray      # int64 [R]: nodes generated (|T|, DART notes eq. (9))
+
+
+def dart_tree(draft_logits: np.ndarray, temperature: float = 1.0, k: int = 25, w: int = 20, theta: int = 59,
+              eps: float = 1e-10) -> DartTree:
+    """DART's candidate-tree construction without the n-gram term (DART notes
+    §5.2 and Algorithm 3 steps 1-8, with g == 1; reading R15):
+
+      p_i = softmax(draft_logits[:, i-1] / T) for the future offsets i = 1..d;
+      active paths C = {root, score 0}; for i = 1..d: K_i = the top-k tokens of
+      p_i (lower id first on equal p); every path in C (in its order) is extended
+      by every token of K_i (in K_i's order) with
+        s_new = s_parent + (0.9^i log(p_i(v) + eps) + 0.5 log(1 + eps)) / (i + 1)^0.7   (eq. 10);
+      all extensions enter the node set T; the w best (score descending, then
+      generation order) become C.
+    Node selection (reading R16): key(node) = min(s_node, key(parent)), root key
+    +inf; the theta nodes with the largest key (then smaller depth, then
+    generation order) are taken.  Keys never increase along a path and ties go to
+    the shallower node, so the selection contains every selected node's parents.
+    Linearisation: depth-first preorder from the root, children in selection
+    order; row 0 is the root (the committed prefix)."""
+    x = np.asarray(draft_logits, dtype=np.float64)
+    R, d, V = x.shape
+    out_par = np.full((R, theta + 1), -1, dtype=np.int64)
+    out_tok = np.zeros((R, theta + 1), dtype=np.int64)
+    out_dep = np.zeros((R, theta + 1), dtype=np.int64)
+    out_key = np.full((R, theta + 1), -np.inf)
+    n_nodes = np.zeros(R, dtype=np.int64)
+    n_exp = np.zeros(R, dtype=np.int64)
+    for r in range(R):
+        p = softmax_t(x[r], temperature)                  # [d, V]
+        # nodes: (score, key, depth, parent node id, token); node id = generation order
+        nodes = []
+        active = [(-1, 0.0, math.inf)]                    # (node id, score, key); -1 = root
+        for i in range(1, d + 1):
+            order = sorted(range(V), key=lambda v: (-p[i - 1, v], v))[:k]
+            scale = (i + 1) ** 0.7
+            ext = []
+            for (pid, ps, pk) in active:
+                for v in order:
+                    s = ps + (0.9 ** i * math.log(p[i - 1, v] + eps) + 0.5 * math.log(1.0 + eps)) / scale
+                    nid = len(nodes)
+                    nodes.append((s, min(s, pk), i, pid, v))
+                    ext.append((nid, s, min(s, pk)))
+            ext.sort(key=lambda e: (-e[1], e[0]))
+            active = ext[:w]
+        sel = sorted(range(len(nodes)), key=lambda n: (-nodes[n][1], nodes[n][2], n))[:theta]
+        chosen = set(sel)
+        rank = {n: j for j, n in enumerate(sel)}
+        children = {}
+        for n in sel:
+            par = nodes[n][3]
+            if par != -1 and par not in chosen:
+                raise AssertionError("selection is not ancestor-closed")
+            children.setdefault(par, []).append(n)
+        for ch in children.values():
+            ch.sort(key=lambda n: rank[n])
+        # depth-first preorder
+        row = {-1: 0}
+        out_par[r, 0] = -1
+        out_key[r, 0] = math.inf
+        stack = list(reversed(children.get(-1, [])))
+        nxt = 1
+        while stack:
+            n = stack.pop()
+            row[n] = nxt
+            out_par[r, nxt] = row[nodes[n][3]]
+            out_tok[r, nxt] = nodes[n][4]
+            out_dep[r, nxt] = nodes[n][2]
+            out_key[r, nxt] = nodes[n][1]
+            nxt += 1
+            stack.extend(reversed(children.get(n, [])))
+        n_nodes[r] = nxt
+        n_exp[r] = len(nodes)
+    return DartTree(out_par, out_tok, n_nodes, out_dep, out_key, n_exp)
 
 
 def prune_threshold(conf: np.ndarray, threshold: float) -> np.ndarray:

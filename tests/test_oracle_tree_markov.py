@@ -6,6 +6,7 @@ all-wrong tree.  Markov head: W1 = 0 gives U exactly, an explicit V x V matrix
 B = W1 W2 built by loops, chi-square of the sampled pair (x_1, x_2) against
 p_1(x_1) p_2(x_2 | x_1), and the pages' two-position worked example.
 """
+import itertools
 import json
 import os
 
@@ -201,3 +202,72 @@ def test_markov_two_position_worked_example():
         assert abs(independent[pair] - val) < 1e-12
     off = sum(v for k, v in independent.items() if gold["joint"][k] == 0.0)
     assert abs(off - gold["product_mass_off_support"]) < 1e-12
+
+
+# --------------------------------------------------------------------------- DART tree construction
+def _delta(p, i, v, eps=1e-10):
+    """eq. (10) with g = 1, restated for the pins."""
+    return (0.9 ** i * np.log(p[i - 1, v] + eps) + 0.5 * np.log(1.0 + eps)) / (i + 1) ** 0.7
+
+
+def test_dart_tree_without_pruning_is_the_brute_force_selection():
+    """w large enough that no path is dropped: T is every path over the per-offset
+    top-k, and the tree is the theta largest bottleneck keys (ties: shallower),
+    computed here by enumerating the paths."""
+    rng = np.random.default_rng(61)
+    d, V, k, theta = 3, 9, 3, 10
+    x = rng.normal(size=(1, d, V)) * 2.0
+    t = oracle.dart_tree(x, 1.0, k=k, w=k ** d, theta=theta)
+    p = scipy.special.softmax(x[0], axis=-1)
+    tops = [list(np.argsort(-p[i], kind="stable")[:k]) for i in range(d)]
+    paths = []                                               # (key, depth, tokens)
+    for depth in range(1, d + 1):
+        for combo in itertools.product(*tops[:depth]):
+            s, key = 0.0, np.inf
+            for i, v in enumerate(combo, start=1):
+                s += _delta(p, i, v)
+                key = min(key, s)
+            paths.append((key, depth, combo))
+    assert t.n_expanded[0] == len(paths) == k + k ** 2 + k ** 3
+    best = sorted(paths, key=lambda e: (-e[0], e[1]))[:theta]
+    # rebuild each selected node's token path from the linearised tree
+    got = []
+    for i in range(1, t.n_nodes[0]):
+        toks, j = [], i
+        while j > 0:
+            toks.append(int(t.tokens[0, j]))
+            j = int(t.parents[0, j])
+        got.append(tuple(reversed(toks)))
+    assert sorted(got) == sorted(tuple(int(v) for v in c) for _, _, c in best)
+    np.testing.assert_allclose(sorted(t.key[0, 1:], reverse=True), [b[0] for b in best], rtol=1e-12)
+
+
+def test_dart_tree_beam_of_one_is_the_argmax_chain_with_its_siblings():
+    rng = np.random.default_rng(62)
+    d, V, k = 4, 20, 3
+    x = rng.normal(size=(1, d, V)) * 3.0
+    t = oracle.dart_tree(x, 1.0, k=k, w=1, theta=d * k)
+    assert t.n_expanded[0] == k * d and t.n_nodes[0] == d * k + 1
+    # along the chain the parent of every depth-(i+1) node is the depth-i argmax
+    g = np.argmax(x[0], axis=-1)
+    for i in range(1, t.n_nodes[0]):
+        dep = t.depth[0, i]
+        par = t.parents[0, i]
+        if dep > 1:
+            assert t.depth[0, par] == dep - 1 and t.tokens[0, par] == g[dep - 2]
+
+
+def test_dart_tree_expansion_bound_closure_and_key_order():
+    """eq. (9): |T| = k + (d-1) w k once each level has w paths; parents precede
+    children; keys never increase along a path; depth <= d."""
+    x = 3.0 * synth.normal(63, 1, (2, 8, 500))
+    t = oracle.dart_tree(x, 1.0, k=25, w=20, theta=59)
+    assert (t.n_expanded == 25 + 7 * 20 * 25).all()          # 3525, the notes' bound met with equality
+    assert (t.n_nodes == 60).all()
+    for r in range(2):
+        for i in range(1, 60):
+            par = t.parents[r, i]
+            assert 0 <= par < i
+            assert t.depth[r, i] == t.depth[r, par] + 1 or par == 0 and t.depth[r, i] == 1
+            assert t.key[r, i] <= t.key[r, par]
+        assert t.depth[r].max() <= 8
