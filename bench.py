@@ -489,6 +489,24 @@ def run_workload(args):
         ms, clocks = _timed(call, None, args.steps, args.warmup, stream)
         launches = 1
         roof = {"bound": "latency", "achieved": None, "peak": None, "unit": None, "traffic": None, "kernel": kernel}
+    elif w == "dart":
+        Rt, dt_, Vt, kt, wt, tht = 16, 8, 151936, 25, 20, 59
+        xt = bf(synth.make_logits(3.0 * synth.normal(8, 1, (Rt, dt_, Vt)), "bf16"))
+        par = torch.empty(Rt, tht + 1, dtype=torch.int32, device=dev)
+        tokt = torch.empty(Rt, tht + 1, dtype=torch.int32, device=dev)
+        nn = torch.empty(Rt, dtype=torch.int32, device=dev)
+        nb = specv.specv_dart_tree_workspace_size(Rt, dt_, Vt, kt, wt, tht, specv.SPECV_BF16)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        call = lambda: check(specv.specv_dart_tree(xt.data_ptr(), specv.SPECV_BF16, Rt, dt_, Vt, 1.0, kt, wt, tht,
+                                                   par.data_ptr(), tokt.data_ptr(), nn.data_ptr(), ws.data_ptr(), nb,
+                                                   sp), "specv_dart_tree")
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        algo = Rt * dt_ * Vt * 2
+        units, unit, metric = Rt, "trees/s", "DART candidate-tree construction: trees/sec"
+        desc, launches, kernel = ("DART tree: R=16, d=8 offsets, V=151936 bf16, top-25, beam 20, 59 nodes", 2,
+                                  "dart_topk_tiles + dart_build")
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
     elif w == "confidence":
         Rc, Gc, Hc, Vc, rank = 512, 7, 4096, 129280, 256
         hc = bf(synth.make_logits(synth.normal(7, 1, (Rc, Gc, Hc)), "bf16"))
@@ -575,7 +593,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "confidence", "dspark"])
+                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "confidence", "dart", "dspark"])
     ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     if args.requests != R:

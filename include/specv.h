@@ -9,6 +9,7 @@
  *                             rejection / residual or bonus token) and, at
  *                             temperature 0, greedy argmax verification
  *   specv_verify_tree_greedy  greedy verification of a linearised candidate tree
+ *   specv_dart_tree           DART's candidate tree (top-k per offset, beam, node budget)
  *   specv_markov_draft        the DSpark Markov draft head, sampled position by position
  *   specv_tv_accept           the analytic acceptance c* = 1 - 1/2 ||p_d - p_t||_1
  *   specv_schedule            DSpark's greedy throughput scheduler
@@ -221,6 +222,42 @@ SPECV_API specv_status specv_verify_tree_greedy(const void* target_logits, specv
                                       int R, int N, int V, int max_depth,
                                       int32_t* path_len, int32_t* path_nodes, int32_t* out_token,
                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ candidate tree */
+
+/*
+ * specv_dart_tree -- DART's candidate-tree construction without the n-gram
+ * index [DART notes §5.2-5.3 and Algorithm 3 steps 1-8, with the n-gram score
+ * g == 1]: for future offsets i = 1..d, K_i = the top-k tokens of
+ * p_i = softmax(draft_logits[:, i-1] / T) (lower id first on equal logits);
+ * starting from the root (score 0) every active path is extended by every token
+ * of K_i with eq. (10)'s increment
+ *   (0.9^i ln(p_i(v) + eps) + 0.5 ln(1 + eps)) / (i + 1)^0.7,   eps = 1e-10,
+ * all extensions join the node set T (at most k + (d-1) w k nodes, eq. (9)) and
+ * the w best (score, then generation order) stay active.  The theta nodes of T
+ * with the largest key = min(score, parent's key) (then smaller depth, then
+ * generation order) form the tree, which is ancestor-closed by construction.
+ * Output, ready for specv_verify_tree_greedy: row 0 is the root (the committed
+ * prefix, parents -1, token 0); rows 1 .. n_nodes-1 are the selected nodes in
+ * depth-first preorder, children in selection order; parents[i] < i.
+ *   draft_logits [R, d, V] dtype, 16-byte aligned rows (V a multiple of 8 for
+ *     bf16, 4 for float32), at most 128 tiles of 2560 (bf16) / 1280 (float32)
+ *     elements per row; T > 0.
+ *   1 <= d <= 8, 1 <= k <= min(32, V), 1 <= w <= 32, 1 <= theta <= 1023; T's
+ *     nodes and the selection frontier must fit 200 KB of shared memory (the
+ *     default (d, k, w, theta) = (8, 25, 20, 59) uses 119 KB).
+ *   parents, tokens [R, theta + 1] int32 out (rows past n_nodes: -1 and 0);
+ *   n_nodes [R] int32 out (= min(theta, |T|) + 1).
+ *   Workspace: specv_dart_tree_workspace_size bytes (0 means unsupported).
+ * Errors: SPECV_ERR_INVALID_ARG for arguments outside these ranges, T <= 0 or
+ *   a short workspace; SPECV_ERR_UNSUPPORTED for unaligned rows or a shape over
+ *   the tile / shared-memory limits.
+ */
+SPECV_API size_t specv_dart_tree_workspace_size(int R, int d, int V, int k, int w, int theta, specv_dtype dtype);
+SPECV_API specv_status specv_dart_tree(const void* draft_logits, specv_dtype dtype, int R, int d, int V,
+                                       float temperature, int k, int w, int theta, int32_t* parents,
+                                       int32_t* tokens, int32_t* n_nodes, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------ Markov head */
 

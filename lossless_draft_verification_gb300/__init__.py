@@ -26,7 +26,8 @@ __all__ = [
     "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_verify_chain_noalloc", "specv_tv_accept_workspace_size", "specv_tv_accept",
     "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
     "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_schedule_global", "specv_prune_threshold",
-    "specv_confidence_head_workspace_size", "specv_confidence_head",
+    "specv_confidence_head_workspace_size", "specv_confidence_head", "specv_dart_tree_workspace_size",
+    "specv_dart_tree",
     "specv_read_device_error",
     "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
     "specv_shard_argmax_combine",
@@ -61,6 +62,9 @@ EXPORTED = {
     "specv_schedule_global": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "specv_prune_threshold": (_c_int, [_vp, _c_int, _c_int, _c_double, _vp, _vp, _c_size, _vp]),
     "specv_confidence_head_workspace_size": (_c_size, [_c_int, _c_int]),
+    "specv_dart_tree_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "specv_dart_tree": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                 _vp, _c_size, _vp]),
     "specv_confidence_head": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                        _vp, _c_size, _vp]),
     "specv_read_device_error": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
@@ -179,6 +183,16 @@ def specv_confidence_head(h, W1, w, b, anchor, draft_tokens, R, gamma, H, V, ran
                           stream):
     return _call("specv_confidence_head", h, W1, w, b, anchor, draft_tokens, R, gamma, H, V, rank, conf, workspace,
                  workspace_bytes, stream)
+
+
+def specv_dart_tree_workspace_size(R, d, V, k, w, theta, dtype):
+    return _call("specv_dart_tree_workspace_size", R, d, V, k, w, theta, dtype)
+
+
+def specv_dart_tree(draft_logits, dtype, R, d, V, temperature, k, w, theta, parents, tokens, n_nodes, workspace,
+                    workspace_bytes, stream):
+    return _call("specv_dart_tree", draft_logits, dtype, R, d, V, temperature, k, w, theta, parents, tokens, n_nodes,
+                 workspace, workspace_bytes, stream)
 
 
 def specv_read_device_error(workspace, stream, status_out):

@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libspecv.so")
 
-SOURCES = ["abi.cu", "chain.cu", "tree.cu", "markov.cu", "schedule.cu", "noalloc.cu", "shard.cu", "confidence.cu"]
+SOURCES = ["abi.cu", "chain.cu", "tree.cu", "markov.cu", "schedule.cu", "noalloc.cu", "shard.cu", "confidence.cu", "dart.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

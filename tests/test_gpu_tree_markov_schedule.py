@@ -312,6 +312,62 @@ def test_prune_threshold_matches_oracle(lib, R, gamma):
     assert lib.read_device_error(ws) == lib.SPECV_ERR_DEVICE_DATA
 
 
+# --------------------------------------------------------------------------- DART candidate tree
+def _run_dart(lib, logits, dtype, T, k, w, theta):
+    import torch
+    dev = torch.device("cuda")
+    R, d, V = logits.shape
+    if dtype == "bf16":
+        x = torch.from_numpy(np.ascontiguousarray(logits.raw.view(np.int16))).to(dev)
+        dt = lib.SPECV_BF16
+    else:
+        x = torch.from_numpy(np.ascontiguousarray(logits.raw)).to(dev)
+        dt = lib.SPECV_F32
+    par = torch.empty(R, theta + 1, dtype=torch.int32, device=dev)
+    tok = torch.empty(R, theta + 1, dtype=torch.int32, device=dev)
+    nn = torch.empty(R, dtype=torch.int32, device=dev)
+    nb = lib.specv_dart_tree_workspace_size(R, d, V, k, w, theta, dt)
+    assert nb > 0
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    st = lib.specv_dart_tree(x.data_ptr(), dt, R, d, V, T, k, w, theta, par.data_ptr(), tok.data_ptr(), nn.data_ptr(),
+                             ws.data_ptr(), nb, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    return par.cpu().numpy(), tok.cpu().numpy(), nn.cpu().numpy()
+
+
+@pytest.mark.parametrize("R,d,V,k,w,theta,dtype,T", [
+    (3, 8, 151936, 25, 20, 59, "bf16", 1.0),       # the notes' (d, k, w, theta)
+    (4, 8, 2048, 25, 20, 59, "f32", 1.0),
+    (2, 3, 512, 4, 2, 11, "bf16", 0.7),
+    (1, 1, 64, 5, 3, 3, "f32", 1.0),
+    (2, 5, 1024, 32, 32, 200, "bf16", 1.0),
+])
+def test_dart_tree_matches_oracle(lib, R, d, V, k, w, theta, dtype, T):
+    logits = synth.make_logits(3.0 * synth.normal(70 + d + k, 1, (R, d, V)), dtype)
+    par, tok, nn = _run_dart(lib, logits, dtype, T, k, w, theta)
+    ref = oracle.dart_tree(logits.f64, T, k=k, w=w, theta=theta)
+    assert (nn == ref.n_nodes).all()
+    assert (par == ref.parents).all()
+    assert (tok == ref.tokens).all()
+
+
+def test_dart_tree_feeds_the_tree_verifier(lib):
+    """The constructed tree goes straight into specv_verify_tree_greedy."""
+    import torch
+    dev = torch.device("cuda")
+    R, d, V = 2, 8, 4096
+    logits = synth.make_logits(3.0 * synth.normal(77, 1, (R, d, V)), "bf16")
+    par, tok, nn = _run_dart(lib, logits, "bf16", 1.0, 25, 20, 59)
+    target = synth.make_logits(3.0 * synth.normal(78, 1, (R, 60, V)), "bf16")
+    ref = oracle.verify_tree_greedy(target.f64, par.astype(np.int64), tok.astype(np.int64), 8)
+    path_len, path, token = lib.verify_tree_greedy(
+        torch.from_numpy(np.ascontiguousarray(target.raw.view(np.int16))).to(dev).view(torch.bfloat16),
+        to_torch(par, dev, np.int32), to_torch(tok, dev, np.int32), 8)
+    assert (path_len.cpu().numpy() == ref.path_len).all()
+    assert (token.cpu().numpy() == ref.token).all()
+
+
 # --------------------------------------------------------------------------- confidence head
 def _conf_case(seed, R, gamma, H, V, rank):
     h = synth.make_logits(synth.normal(seed, 1, (R, gamma, H)), "bf16")
