@@ -151,14 +151,12 @@ __device__ __forceinline__ bool dart_better(unsigned long long ka, int da, int i
 __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuildArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   DartNode* T = reinterpret_cast<DartNode*>(smem);                 // [k + (d - 1) w k]
-  int* front = reinterpret_cast<int*>(T + (a.k + (a.d - 1) * a.w * a.k));   // [k + theta k]
   __shared__ int s_tok[kDartMaxDepth][kDartMaxK];
   __shared__ double s_lp[kDartMaxDepth][kDartMaxK];
   __shared__ int s_active[kDartMaxW];
-  __shared__ int s_nfront;
   __shared__ int s_sel[kDartMaxTheta];
-  __shared__ unsigned long long s_bk[kDartBuildThreads / 32];
-  __shared__ int s_bd[kDartBuildThreads / 32], s_bi[kDartBuildThreads / 32], s_bq[kDartBuildThreads / 32];
+  __shared__ int s_lbase[kDartMaxTheta + 1], s_lhead[kDartMaxTheta + 1];
+  __shared__ int s_nlist;
   const int r = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = a.d, k = a.k, w = a.w;
@@ -182,71 +180,77 @@ __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuild
     // l owns tiles l, l + 32, l + 64, l + 96 and the head index of each
     const DartCand* c = a.cand + row * a.ntile * k;
     int head[kDartMaxTilesPerLane];
+    DartCand hc[kDartMaxTilesPerLane];                       // each owned tile's current head
 #pragma unroll
-    for (int u = 0; u < kDartMaxTilesPerLane; ++u) head[u] = 0;
+    for (int u = 0; u < kDartMaxTilesPerLane; ++u) {
+      head[u] = 0;
+      const int tile = lane + 32 * u;
+      hc[u] = tile < a.ntile ? c[size_t(tile) * k] : DartCand{neg_inf(), 0x7fffffff};
+    }
+    float px = 0.f;                                          // lane t: logit of pick t
     for (int t = 0; t < k; ++t) {
       float bv = neg_inf();
       int bi = 0x7fffffff, bu = -1;
 #pragma unroll
       for (int u = 0; u < kDartMaxTilesPerLane; ++u) {
-        const int tile = lane + 32 * u;
-        if (tile < a.ntile && head[u] < k) {
-          const DartCand x = c[size_t(tile) * k + head[u]];
-          if (x.i != 0x7fffffff && (x.v > bv || (x.v == bv && x.i < bi))) { bv = x.v; bi = x.i; bu = u; }
-        }
+        const DartCand x = hc[u];
+        if (x.i != 0x7fffffff && (x.v > bv || (x.v == bv && x.i < bi))) { bv = x.v; bi = x.i; bu = u; }
       }
       const int mine = bi;
       warp_argmax(bv, bi);                      // all lanes take part
       if (bi != 0x7fffffff && mine == bi) {     // the owner of the pick advances that tile
 #pragma unroll
         for (int u = 0; u < kDartMaxTilesPerLane; ++u)
-          if (u == bu) ++head[u];
+          if (u == bu) {
+            ++head[u];
+            hc[u] = head[u] < k ? c[size_t(lane + 32 * u) * k + head[u]] : DartCand{neg_inf(), 0x7fffffff};
+          }
       }
-      if (lane == 0) {
-        s_tok[i][t] = bi;
-        const double lp = bi == 0x7fffffff ? -INFINITY : (double(bv) * a.c2 - lse2) * 0.6931471805599453;
-        s_lp[i][t] = log(exp(lp) + a.eps);
-      }
+      if (lane == t) px = bv;
+      if (lane == 0) s_tok[i][t] = bi;
+    }
+    __syncwarp();
+    if (lane < k) {                             // ln(p + eps) of every pick at once
+      const int t = lane;
+      const double lp = s_tok[i][t] == 0x7fffffff ? -INFINITY : (double(px) * a.c2 - lse2) * 0.6931471805599453;
+      s_lp[i][t] = log(exp(lp) + a.eps);
     }
   }
   __syncthreads();
 
-  // ---- beam over depths.  T[0 .. k) are the root's children; at depth i >= 2
-  // the active paths (in their rank order) are extended, each by the k picks of
-  // offset i in order, so path j's children are T[base + j k .. + k).
-  const double scale1 = pow(2.0, 0.7);
-  const double ng = 0.5 * log(1.0 + a.eps);
-  for (int t = tid; t < k; t += kDartBuildThreads) {
-    const double s = (0.9 * s_lp[0][t] + ng) / scale1;
-    DartNode n;
-    n.score = s;
-    n.s_ord = dart_ord(s);
-    n.k_ord = n.s_ord;
-    n.parent = -1;
-    n.token = s_tok[0][t];
-    n.depth = 1;
-    n.child0 = -1;
-    T[t] = n;
-  }
   __syncthreads();
-  int base = 0, count = k;                   // the last depth's nodes in T
-  for (int i = 2; i <= d + 1; ++i) {
-    // rank the last depth's nodes by (score desc, generation order); the w best are active
-    for (int q = tid; q < count; q += kDartBuildThreads) {
-      const unsigned long long sq = T[base + q].s_ord;
-      int rank = 0;
-      for (int u = 0; u < count; ++u) {
-        const unsigned long long su = T[base + u].s_ord;
-        rank += (su > sq || (su == sq && u < q)) ? 1 : 0;
-      }
-      if (rank < w) s_active[rank] = base + q;
+  if (warp != 0) return;
+  // Everything below runs in warp 0: the beam and the selection are merges of
+  // lists that are already ordered, so no block barrier is needed.
+  //
+  // ---- beam over depths.  T[0 .. k) are the root's children; at depth i >= 2
+  // active path j's k extensions are T[nb + j k .. + k).  A path's extensions
+  // come in the order of its offset's picks, i.e. by non-increasing score, so
+  // the w best of a depth are a w-way merge of those lists (lane j owns list j).
+  const double ng = 0.5 * log(1.0 + a.eps);
+  {
+    const double sc1 = pow(2.0, 0.7);
+    for (int t = lane; t < k; t += 32) {
+      const double sv = (0.9 * s_lp[0][t] + ng) / sc1;
+      DartNode n;
+      n.score = sv;
+      n.s_ord = dart_ord(sv);
+      n.k_ord = n.s_ord;
+      n.parent = -1;
+      n.token = s_tok[0][t];
+      n.depth = 1;
+      n.child0 = -1;
+      T[t] = n;
     }
-    __syncthreads();
-    if (i > d) break;
-    const int nact = min(w, count);
+  }
+  int nact = min(w, k);
+  for (int j = lane; j < nact; j += 32) s_active[j] = j;
+  __syncwarp();
+  int base = 0, count = k;
+  for (int i = 2; i <= d; ++i) {
     const int nb = base + count;
     const double pw = pow(0.9, double(i)), sc = pow(double(i + 1), 0.7);
-    for (int q = tid; q < nact * k; q += kDartBuildThreads) {
+    for (int q = lane; q < nact * k; q += 32) {
       const int j = q / k, t = q - j * k;
       const DartNode& par = T[s_active[j]];
       DartNode n;
@@ -259,55 +263,70 @@ __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuild
       n.child0 = -1;
       T[nb + q] = n;
     }
-    for (int j = tid; j < nact; j += kDartBuildThreads) T[s_active[j]].child0 = nb + j * k;
-    __syncthreads();
+    for (int j = lane; j < nact; j += 32) T[s_active[j]].child0 = nb + j * k;
+    __syncwarp();
+    const int nnext = min(w, nact * k);
+    int h = 0;                                                 // lane j: head of list j
+    int pick = -1;
+    for (int p = 0; p < nnext; ++p) {
+      unsigned long long bo = 0;
+      int bg = 0x7fffffff;
+      if (lane < nact && h < k) { bg = nb + lane * k + h; bo = T[bg].s_ord; }
+      unsigned long long wo = bo;
+      int wg = bg;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long oo = __shfl_xor_sync(0xffffffffu, wo, o);
+        const int og = __shfl_xor_sync(0xffffffffu, wg, o);
+        if (oo > wo || (oo == wo && og < wg)) { wo = oo; wg = og; }
+      }
+      if (wg == bg) ++h;                                       // the winning list advances
+      if (lane == p) pick = wg;
+    }
+    if (lane < nnext) s_active[lane] = pick;               // nnext <= w <= 32: lane p holds pick p
+    __syncwarp();
     base = nb;
     count = nact * k;
+    nact = nnext;
   }
   const int total = base + count;
 
-  // ---- best-first selection of theta nodes: the frontier starts with the root's
-  // children; each pick adds its children
-  if (tid == 0) s_nfront = 0;
-  __syncthreads();
-  for (int t = tid; t < k; t += kDartBuildThreads) front[t] = t;
-  if (tid == 0) s_nfront = k;
-  __syncthreads();
+  // ---- best-first selection: a merge of the open child lists.  The root's
+  // list is T[0 .. k); a picked node that was extended opens its k children.
+  // Within a list keys do not increase, and across lists the order is (key
+  // desc, depth asc, generation asc), so every pick is the best node left.
   const int want = min(a.theta, total);
+  if (lane == 0) { s_lbase[0] = 0; s_lhead[0] = 0; s_nlist = 1; }
+  __syncwarp();
   for (int p = 0; p < want; ++p) {
-    const int nf = s_nfront;
+    const int nl = s_nlist;
     unsigned long long bk = 0;
-    int bd = 0x7fffffff, bi = 0x7fffffff, bq = -1;
-    for (int q = tid; q < nf; q += kDartBuildThreads) {
-      const int id = front[q];
-      if (id < 0) continue;
+    int bd = 0x7fffffff, bi = 0x7fffffff, bl = -1;
+    for (int l = lane; l < nl; l += 32) {
+      if (s_lhead[l] >= k) continue;
+      const int id = s_lbase[l] + s_lhead[l];
       const DartNode& n = T[id];
-      if (bq < 0 || dart_better(n.k_ord, n.depth, id, bk, bd, bi)) { bk = n.k_ord; bd = n.depth; bi = id; bq = q; }
+      if (bl < 0 || dart_better(n.k_ord, n.depth, id, bk, bd, bi)) { bk = n.k_ord; bd = n.depth; bi = id; bl = l; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
       const int od = __shfl_xor_sync(0xffffffffu, bd, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int oq = __shfl_xor_sync(0xffffffffu, bq, o);
-      if (oq >= 0 && (bq < 0 || dart_better(ok, od, oi, bk, bd, bi))) { bk = ok; bd = od; bi = oi; bq = oq; }
+      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (ol >= 0 && (bl < 0 || dart_better(ok, od, oi, bk, bd, bi))) { bk = ok; bd = od; bi = oi; bl = ol; }
     }
-    if (lane == 0) { s_bk[warp] = bk; s_bd[warp] = bd; s_bi[warp] = bi; s_bq[warp] = bq; }
-    __syncthreads();
-    if (tid == 0) {
-      for (int u = 1; u < kDartBuildThreads / 32; ++u)
-        if (s_bq[u] >= 0 && (bq < 0 || dart_better(s_bk[u], s_bd[u], s_bi[u], bk, bd, bi))) {
-          bk = s_bk[u]; bd = s_bd[u]; bi = s_bi[u]; bq = s_bq[u];
-        }
+    if (lane == 0) {
       s_sel[p] = bi;
-      front[bq] = -1;                                 // taken
+      ++s_lhead[bl];
       const int c0 = T[bi].child0;
       if (c0 >= 0) {
-        for (int t = 0; t < k; ++t) front[s_nfront + t] = c0 + t;
-        s_nfront += k;
+        s_lbase[s_nlist] = c0;
+        s_lhead[s_nlist] = 0;
+        ++s_nlist;
       }
     }
-    __syncthreads();
+    __syncwarp();
   }
 
   // ---- the tree, depth first from the root, children in selection order.
