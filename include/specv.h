@@ -244,8 +244,8 @@ SPECV_API specv_status specv_verify_tree_greedy(const void* target_logits, specv
  *     bf16, 4 for float32), at most 128 tiles of 2560 (bf16) / 1280 (float32)
  *     elements per row; T > 0.
  *   1 <= d <= 8, 1 <= k <= min(32, V), 1 <= w <= 32, 1 <= theta <= 1023; T's
- *     nodes and the selection frontier must fit 200 KB of shared memory (the
- *     default (d, k, w, theta) = (8, 25, 20, 59) uses 119 KB).
+ *     k + (d-1) w k nodes, 40 bytes each, must fit 200 KB of shared memory
+ *     (the default (d, k, w, theta) = (8, 25, 20, 59) uses 138 KB).
  *   parents, tokens [R, theta + 1] int32 out (rows past n_nodes: -1 and 0);
  *   n_nodes [R] int32 out (= min(theta, |T|) + 1).
  *   Workspace: specv_dart_tree_workspace_size bytes (0 means unsupported).

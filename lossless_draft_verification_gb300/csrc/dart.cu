@@ -10,24 +10,33 @@
 //
 // Kernels
 //   dart_topk_tiles  one warp per (row, warp tile) of the [R, d, V] draft
-//                    logits: the tile's softmax partial (max * c2, sum of
-//                    2^(x c2 - max c2)) and its top-k (logit, id) candidates by
-//                    repeated warp argmax (lowest id among equal logits).  The
-//                    only pass over the logits: HBM-bound.
-//   dart_build       one CTA per request: warp i merges offset i's tile
-//                    candidates into the top-k and forms log p(v) in float64
-//                    from the combined normaliser; the beam over depths ranks
-//                    its w * k candidates by counting (score, then generation
-//                    order); the selection takes, theta times, the best node of
-//                    the frontier (children of the nodes taken so far) by the
-//                    key min(score, parent key), then smaller depth, then
-//                    generation order -- since keys never increase along a path
-//                    and equal keys go to the shallower node, this is the theta
-//                    largest keys of T, ancestor-closed; thread 0 then writes
-//                    the tree depth-first (children in selection order).
+//                    logits, in the only pass over them (HBM-bound): the
+//                    tile's softmax partial (max * c2, sum of 2^(x c2 - max c2))
+//                    and its top-k (logit, id) candidates, lowest id first
+//                    among equal logits.  The k-th best of the 32 lanes' own
+//                    best elements bounds the tile's k-th best from below, so
+//                    only the few values at or above it are compacted to
+//                    shared memory and ranked by counting.  The last warp of a
+//                    row to finish (a ticket per row) merges the row's tile
+//                    lists the same way and forms ln(p(v) + eps) of the row's
+//                    top-k in float64 from the combined normaliser.
+//   dart_build       one CTA per request: eq. (10)'s increment of every
+//                    (offset, pick) once; all threads extend the active paths,
+//                    one warp keeps the w best (a merge of the score-ordered
+//                    extension lists); the selection is one warp's merge of
+//                    all of T's lists by the key min(score, parent key), then
+//                    smaller depth, then generation order -- keys never
+//                    increase along a path and equal keys go to the shallower
+//                    node, so the theta best are ancestor-closed; the tree's
+//                    depth-first rows (children in selection order) come from
+//                    subtree sizes, one barrier per depth.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <cuda_bf16.h>
+#include <type_traits>
 
 #include "common.cuh"
 #include "host_common.h"
@@ -41,11 +50,13 @@ constexpr int kDartMaxW = 32;
 constexpr int kDartMaxDepth = 8;            // one warp per offset in dart_build
 constexpr int kDartMaxTheta = 1023;
 constexpr int kDartVpt = 10;                // slots per lane and row in dart_topk_tiles
-constexpr int kDartMaxTilesPerLane = 4;     // warp tiles per row <= 128
+constexpr int kDartMaxTiles = 128;          // warp tiles per row
+constexpr int kDartSurvCap = 128;           // survivors of the bound ranked in shared memory
+constexpr int kDartNone = 0x7fffffff;       // id of an empty candidate slot
 
 struct DartCand {
   float v;                                  // logit (raw, before 1/T)
-  int i;                                    // token id
+  int i;                                    // token id; kDartNone for an empty slot
 };
 
 struct DartTileArgs {
@@ -54,86 +65,400 @@ struct DartTileArgs {
   DartCand* cand;                           // [R * d, ntile, k]
   long V;
   int rows, ntile, k;
-  float c2;
+  float c2;                                 // log2(e) / T
 };
 
+// (logit descending, id ascending) as one unsigned integer, larger is better;
+// 0 is below every element.  -0 is taken as +0, as the float comparison does.
+__device__ __forceinline__ unsigned long long dart_key(float v, int id) {
+  uint32_t b = __float_as_uint(v);
+  b = b == 0x80000000u ? 0u : b;
+  const uint32_t o = b ^ (uint32_t(int32_t(b) >> 31) | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | (~static_cast<uint32_t>(id));
+}
+
+__device__ __forceinline__ DartCand dart_unkey(unsigned long long key) {
+  const uint32_t o = uint32_t(key >> 32);
+  const uint32_t b = (o >> 31) ? (o & 0x7fffffffu) : ~o;
+  return DartCand{__uint_as_float(b), int(~uint32_t(key))};
+}
+
+// the k-th largest (1 <= k <= 32) of the warp's 32 keys
+__device__ __forceinline__ unsigned long long warp_kth_largest(unsigned long long key, int k, int lane) {
+  int rank = 0;                             // lanes above, equal keys ordered by lane
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const unsigned long long o = __shfl_sync(0xffffffffu, key, l);
+    rank += (o > key || (o == key && l < lane)) ? 1 : 0;
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, rank == k - 1);
+  return __shfl_sync(0xffffffffu, key, __ffs(m) - 1);
+}
+
+// exclusive prefix of c over the warp; *total gets the sum
+__device__ __forceinline__ int warp_excl_scan(int c, int lane, int* total) {
+  int inc = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  *total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - c;
+}
+
+// Rank the n <= kDartSurvCap distinct keys s[0 .. n) by counting; the entry of
+// rank t < k goes to out(t, key).  EPL entries per lane.
+template <int EPL, typename Key, typename Out>
+__device__ __forceinline__ void dart_rank(const Key* s, int n, int k, int lane, Out out) {
+  Key x[EPL];
+  int r[EPL];
+#pragma unroll
+  for (int u = 0; u < EPL; ++u) {
+    x[u] = lane + 32 * u < n ? s[lane + 32 * u] : Key(0);
+    r[u] = 0;
+  }
+  for (int y = 0; y < n; ++y) {
+    const Key o = s[y];
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) r[u] += o > x[u] ? 1 : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < EPL; ++u)
+    if (lane + 32 * u < n && r[u] < k) out(r[u], x[u]);
+}
+
+template <typename Key, typename Out>
+__device__ __forceinline__ void dart_rank_any(const Key* s, int n, int k, int lane, Out out) {
+  if (n <= 32) dart_rank<1>(s, n, k, lane, out);
+  else if (n <= 64) dart_rank<2>(s, n, k, lane, out);
+  else dart_rank<4>(s, n, k, lane, out);
+}
+
+// bf16 candidates of one tile as 32 bits: the logit's order-preserving image
+// (-0 taken as +0) above 0xffff minus the element's place in the tile (< 2560)
+__device__ __forceinline__ uint32_t dart_key16(uint32_t h, int loc) {
+  h = h == 0x8000u ? 0u : h;
+  const uint32_t o = (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+  return (o << 16) | (0xffffu - uint32_t(loc));
+}
+
+__device__ __forceinline__ DartCand dart_unkey16(uint32_t key, int tile_base) {
+  const uint32_t o = key >> 16;
+  const uint32_t h = (o & 0x8000u) ? (o & 0x7fffu) : (~o & 0xffffu);
+  return DartCand{__uint_as_float(h << 16), tile_base + int(0xffffu - (key & 0xffffu))};
+}
+
+// the k-th largest (1 <= k <= 32) of the warp's 32 values, equal values
+// counted once per lane
+__device__ __forceinline__ float warp_kth_largest_f(float v, int k, int lane) {
+  int rank = 0;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) {
+    const float o = __shfl_sync(0xffffffffu, v, l);
+    rank += (o > v || (o == v && l < lane)) ? 1 : 0;
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, rank == k - 1);
+  return __shfl_sync(0xffffffffu, v, __ffs(m) - 1);
+}
+
+// One warp merges a row's tile results: the combined normaliser and the top-k
+// of the row's ntile * k candidates; emit(t, id, ln(p(v) + eps)) for t < k.
+template <typename Emit>
+__device__ __forceinline__ void dart_row_merge(const float2* part, const DartCand* cand, int ntile, int k, double c2d,
+                                               double le, int row, unsigned long long* surv, int lane, Emit out) {
+  const float2* pt = part + size_t(row) * ntile;
+  float M = neg_inf();
+  for (int t = lane; t < ntile; t += 32) M = fmaxf(M, __ldg(pt + t).x);
+  M = warp_max(M);
+  // sum of the partials in float64 (the terms themselves carry float32
+  // rounding already: float32 2^x is as good), log2 as exponent + float32
+  // log2 of the mantissa in [1, 2)
+  double Z = 0.0;
+  for (int t = lane; t < ntile; t += 32) {
+    const float2 q = __ldg(pt + t);
+    if (q.y > 0.f) Z += double(q.y) * double(exp2f(q.x - M));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+  int ze;
+  const double zm = frexp(Z, &ze);                          // Z = zm 2^ze, zm in [0.5, 1)
+  const double lse2 = double(M) + double(ze - 1) + double(log2f(float(2.0 * zm)));
+  const int nall = ntile * k;
+  const int2* c = reinterpret_cast<const int2*>(cand + size_t(row) * nall);
+  auto key_at = [&](int e) -> unsigned long long {
+    const int2 q = __ldg(c + e);
+    return q.y == kDartNone ? 0ull : dart_key(__int_as_float(q.x), q.y);
+  };
+  // ln(p + eps) = max(ln p, ln eps) + ln(1 + e^-|ln p - ln eps|) (le = ln eps):
+  // ln p in float64, the bounded correction term in float32
+  auto emit = [&](int t, unsigned long long key) {
+    const DartCand x = key ? dart_unkey(key) : DartCand{neg_inf(), kDartNone};
+    const double lp = x.i == kDartNone ? -INFINITY : (double(x.v) * c2d - lse2) * 0.6931471805599453;
+    const double hi = lp > le ? lp : le;
+    const float gap = lp > le ? float(le - lp) : float(lp - le);           // <= 0
+    out(t, x.i, hi + double(log1pf(expf(gap))));
+  };
+  // Each tile's list is in key order, so its head is its best: the k-th best
+  // of the lanes' best heads (lane l owns tiles l, l + 32, ...) comes from k
+  // distinct candidates and bounds the row's k-th best from below.  Only each
+  // list's prefix at or above the bound is kept.
+  constexpr int kOwn = kDartMaxTiles / 32;
+  unsigned long long best = 0;
+#pragma unroll
+  for (int u = 0; u < kOwn; ++u) {
+    const int t = lane + 32 * u;
+    if (t < ntile) best = max(best, key_at(t * k));
+  }
+  const unsigned long long thr = warp_kth_largest(best, k, lane);
+  int len[kOwn];
+  int cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kOwn; ++u) {
+    const int t = lane + 32 * u;
+    int h = 0;
+    if (t < ntile) {
+      // walk the prefix four candidates at a time (independent loads)
+      bool more = true;
+      while (more && h < k) {
+        unsigned long long x[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[v] = h + v < k ? key_at(t * k + h + v) : 0ull;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          if (more && x[v] != 0 && x[v] >= thr) ++h;
+          else more = false;
+        }
+      }
+    }
+    len[u] = h;
+    cnt += h;
+  }
+  int n;
+  int pos = warp_excl_scan(cnt, lane, &n);
+  if (n <= kDartSurvCap) {
+#pragma unroll
+    for (int u = 0; u < kOwn; ++u) {
+      const int t = lane + 32 * u;
+      for (int h = 0; h < len[u]; ++h) surv[pos++] = key_at(t * k + h);
+    }
+    __syncwarp();
+    dart_rank_any(surv, n, k, lane, emit);
+    for (int t = n + lane; t < k; t += 32) emit(t, 0ull);
+    return;
+  }
+  // many candidates at the bound (ties): k rounds of the largest key below the last
+  constexpr int kChunk = 16;
+  unsigned long long prev = ~0ull;
+  for (int t = 0; t < k; ++t) {
+    unsigned long long b = 0;
+    for (int e0 = 0; e0 < nall; e0 += 32 * kChunk) {
+      unsigned long long x[kChunk];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        const int e = e0 + 32 * u + lane;
+        x[u] = e < nall ? key_at(e) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u)
+        if (x[u] < prev) b = max(b, x[u]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    if (lane == t) emit(t, b);
+    prev = b;                                 // 0 once the candidates run out
+  }
+}
+
+__device__ __forceinline__ __nv_bfloat162 dart_as_b2(uint32_t u) {
+  __nv_bfloat162 b;
+  memcpy(&b, &u, sizeof(b));
+  return b;
+}
+
 template <typename Elem>
-__global__ void __launch_bounds__(kDartTileWarps * 32) dart_topk_tiles_kernel(DartTileArgs a) {
+__global__ void __launch_bounds__(kDartTileWarps * 32, 2) dart_topk_tiles_kernel(DartTileArgs a) {
   using S = Slot<Elem, true>;
   constexpr int VW = S::VW;
-  const int lane = threadIdx.x & 31;
-  const long unit = long(blockIdx.x) * kDartTileWarps + (threadIdx.x >> 5);
+  constexpr int NE = kDartVpt * VW;                          // elements per lane
+  constexpr int MW = (NE + 31) / 32;                         // survivor-mask words
+  constexpr bool kB16 = VW == 8;
+  using Key = typename std::conditional<kB16, uint32_t, unsigned long long>::type;
+  extern __shared__ __align__(16) unsigned char dsm[];      // per warp: the tile, in row order
+  __shared__ unsigned long long s_surv[kDartTileWarps][kDartSurvCap];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long unit = long(blockIdx.x) * kDartTileWarps + warp;
   if (unit >= long(a.rows) * a.ntile) return;
   const int row = int(unit / a.ntile), tile = int(unit - long(row) * a.ntile);
+  const int tile_base = tile * (32 * kDartVpt * VW);
   const Elem* x = reinterpret_cast<const Elem*>(a.logits) + size_t(row) * size_t(a.V);
-  float val[kDartVpt * VW];
+  uint4* cp = reinterpret_cast<uint4*>(dsm) + warp * (kDartVpt * 32);
+  S sl[kDartVpt];                                            // the lane's slots, kept packed
 #pragma unroll
-  for (int j = 0; j < kDartVpt; ++j) {
-    S s;
-    s.load(x, slot_index<kDartVpt, VW>(tile, j, lane), a.V);
+  for (int j = 0; j < kDartVpt; ++j) sl[j].load(x, slot_index<kDartVpt, VW>(tile, j, lane), a.V);
 #pragma unroll
-    for (int e = 0; e < VW; ++e) val[j * VW + e] = s.get(e);
+  for (int j = 0; j < kDartVpt; ++j) cp[j * 32 + lane] = make_uint4(sl[j].w[0], sl[j].w[1], sl[j].w[2], sl[j].w[3]);
+  // the lane's largest logit (slots past the row read -inf; NaN never wins)
+  float lv;
+  if constexpr (kB16) {
+    __nv_bfloat162 mx = __float2bfloat162_rn(neg_inf());
+#pragma unroll
+    for (int j = 0; j < kDartVpt; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx = __hmax2(mx, dart_as_b2(sl[j].w[i]));
+    lv = fmaxf(__low2float(mx), __high2float(mx));
+  } else {
+    lv = neg_inf();
+#pragma unroll
+    for (int j = 0; j < kDartVpt; ++j)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) lv = fmaxf(lv, sl[j].get(e));
   }
-  // softmax partial of the tile
-  float m = neg_inf();
-#pragma unroll
-  for (int q = 0; q < kDartVpt * VW; ++q) m = fmaxf(m, val[q]);
-  m = warp_max(m);
+  // the tile's softmax partial
+  const float m = warp_max(lv);
   float z = 0.f;
   if (m > neg_inf()) {
+    const float2 c2 = make_float2(a.c2, a.c2), nm = make_float2(-m * a.c2, -m * a.c2);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < kDartVpt * VW; ++q) z += ex2(fmaf(val[q], a.c2, -m * a.c2));
+    for (int j = 0; j < kDartVpt; ++j)
+#pragma unroll
+      for (int e = 0; e < VW; e += 2) {
+        const float2 r = fma2(make_float2(sl[j].get(e), sl[j].get(e + 1)), c2, nm);
+        acc = add2(acc, make_float2(ex2(r.x), ex2(r.y)));
+      }
+    z = acc.x + acc.y;
   }
   z = warp_sum(z);
   if (lane == 0) a.part[unit] = make_float2(m > neg_inf() ? m * a.c2 : neg_inf(), z);
-  // top-k by repeated argmax; the winning element is struck out
-  for (int t = 0; t < a.k; ++t) {
-    float bv = neg_inf();
-    int bi = 0x7fffffff;
+
+  // The k-th largest of the 32 lane maxima comes from k distinct elements, so
+  // the tile's top-k all have logits >= it: only those elements are kept (a
+  // bit mask per lane, element q = slot * VW + e).
+  const int k = a.k;
+  DartCand* out = a.cand + size_t(unit) * k;
+  const float tv = warp_kth_largest_f(lv, k, lane);
+  uint32_t mk[MW];
 #pragma unroll
-    for (int j = 0; j < kDartVpt; ++j)
+  for (int w = 0; w < MW; ++w) mk[w] = 0u;
+  if constexpr (kB16) {
+    const __nv_bfloat162 t2 = __float2bfloat162_rn(tv);     // exact: tv is one of the logits, or -inf
+#pragma unroll
+    for (int j = 0; j < kDartVpt; ++j) {
+      const bool ok = slot_index<kDartVpt, VW>(tile, j, lane) < a.V;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = ok ? __hge2_mask(dart_as_b2(sl[j].w[i]), t2) : 0u;
+        const int q = j * VW + 2 * i;
+        mk[q >> 5] |= ((c & 1u) | ((c >> 15) & 2u)) << (q & 31);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kDartVpt; ++j) {
+      const bool ok = slot_index<kDartVpt, VW>(tile, j, lane) < a.V;
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        const int id = int(slot_index<kDartVpt, VW>(tile, j, lane)) + e;
-        const float v = val[j * VW + e];
-        if (id < a.V && (v > bv || (v == bv && id < bi))) { bv = v; bi = id; }
+        const int q = j * VW + e;
+        if (ok && sl[j].get(e) >= tv) mk[q >> 5] |= 1u << (q & 31);
       }
-    warp_argmax(bv, bi);
+    }
+  }
+  int cnt = 0;
 #pragma unroll
-    for (int j = 0; j < kDartVpt; ++j)
+  for (int w = 0; w < MW; ++w) cnt += __popc(mk[w]);
+  int n;
+  int pos = warp_excl_scan(cnt, lane, &n);
+  unsigned long long* surv = s_surv[warp];
+  if (n <= kDartSurvCap) {
+    Key* sk = reinterpret_cast<Key*>(surv);
+    const Elem* te = reinterpret_cast<const Elem*>(cp);     // te[loc]: the tile's element loc
 #pragma unroll
-      for (int e = 0; e < VW; ++e)
-        if (int(slot_index<kDartVpt, VW>(tile, j, lane)) + e == bi) val[j * VW + e] = neg_inf();
-    if (lane == 0) {
-      DartCand c;
-      c.v = bi == 0x7fffffff ? neg_inf() : bv;
-      c.i = bi;
-      a.cand[size_t(unit) * a.k + t] = c;
+    for (int w = 0; w < MW; ++w) {
+      uint32_t b = mk[w];
+      while (b) {
+        const int q = w * 32 + __ffs(b) - 1;
+        b &= b - 1;
+        const int loc = ((q / VW) * 32 + lane) * VW + (q % VW);
+        if constexpr (kB16) sk[pos++] = dart_key16(reinterpret_cast<const uint16_t*>(te)[loc], loc);
+        else sk[pos++] = dart_key(te[loc], tile_base + loc);
+      }
+    }
+    __syncwarp();
+    dart_rank_any(sk, n, k, lane, [&](int t, Key key) {
+      if constexpr (kB16) out[t] = dart_unkey16(key, tile_base);
+      else out[t] = dart_unkey(key);
+    });
+    for (int t = n + lane; t < k; t += 32) out[t] = DartCand{neg_inf(), kDartNone};
+  } else {
+    // many values tie at the bound: k rounds of the largest key below the
+    // last, over the tile read again (a rare path, kept off the registers of
+    // the main one)
+    unsigned long long prev = ~0ull;
+    for (int t = 0; t < k; ++t) {
+      unsigned long long b = 0;
+#pragma unroll 1
+      for (int j = 0; j < kDartVpt; ++j) {
+        const long base = slot_index<kDartVpt, VW>(tile, j, lane);
+        if (base >= a.V) break;               // slots only grow with j
+        S q;
+        q.load(x, base, a.V);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float v = q.get(e);
+          const unsigned long long key = dart_key(v, int(base) + e);
+          if (v == v && key < prev) b = max(b, key);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+      if (lane == t) out[t] = b ? dart_unkey(b) : DartCand{neg_inf(), kDartNone};
+      prev = b;                               // 0 once the tile runs out
     }
   }
 }
 
 struct DartBuildArgs {
-  const float2* part;
-  const DartCand* cand;
+  const float2* part;                       // [R * d, ntile] tile softmax partials
+  const DartCand* cand;                     // [R * d, ntile, k] tile top-k lists
   int32_t* parents;                         // [R, theta + 1]
   int32_t* tokens;                          // [R, theta + 1]
   int32_t* n_nodes;                         // [R]
   void* workspace;
-  int d, ntile, k, w, theta;
-  double c2;                                // log2(e) / T
-  double eps;
+  int d, k, w, theta;
+  int nodes;                                // k + (d - 1) w k: T's capacity
+  int ntile;
+  double c2d;                               // log2(e) / T
+  double ln_eps;
+  double ng;                                // 0.5 ln(1 + eps)
+  double pw[kDartMaxDepth];                 // 0.9^i for depth i = 1..d
+  double sc[kDartMaxDepth];                 // (i + 1)^0.7
 };
 
-// node of T in shared memory; its index is its generation order
-struct DartNode {
-  double score;
-  unsigned long long s_ord, k_ord;          // order-preserving integer images of score and key
-  int parent;                               // node index, -1 for the root
-  int token;
-  int depth;
-  int child0;                               // first of its k children in T, -1 if never extended
+// T in shared memory as one array per field (a node's index is its
+// generation order), so that consecutive nodes sit in consecutive banks
+struct DartT {
+  double* score;
+  unsigned long long* s_ord;                // order-preserving image of score
+  unsigned long long* k_ord;                // of the key min(score, parent key)
+  int* parent;                              // node index, -1 for the root
+  int* token;
+  int* depth;
+  int* child0;                              // first of its k children, -1 if never extended
 };
+constexpr int kDartNodeBytes = 3 * 8 + 4 * 4;
+
+__device__ __forceinline__ DartT dart_t_layout(unsigned char* smem, int N) {
+  DartT t;
+  t.score = reinterpret_cast<double*>(smem);
+  t.s_ord = reinterpret_cast<unsigned long long*>(t.score + N);
+  t.k_ord = t.s_ord + N;
+  t.parent = reinterpret_cast<int*>(t.k_ord + N);
+  t.token = t.parent + N;
+  t.depth = t.token + N;
+  t.child0 = t.depth + N;
+  return t;
+}
 
 // An unsigned integer with the order of the double x (x not NaN): comparisons
 // then run on the integer units, not on the narrow float64 pipe.
@@ -142,239 +467,219 @@ __device__ __forceinline__ unsigned long long dart_ord(double x) {
   return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 
-// (key, depth, generation order): larger key first, then shallower, then older
-__device__ __forceinline__ bool dart_better(unsigned long long ka, int da, int ia, unsigned long long kb, int db,
-                                            int ib) {
-  return ka > kb || (ka == kb && (da < db || (da == db && ia < ib)));
+// Selection merge in one warp over the L (<= 256) lists T[li k .. + k), each
+// in (key, depth, generation) order: lane l caches the heads of lists l,
+// l + 32, ...; each pick is the largest (key image, ~(depth << 16 | node)) by
+// three 32-bit warp maxima, and the winning lane advances that list.
+__device__ __forceinline__ void dart_select_merge(const DartT& T, int L, int k, int want, int* sel, int lane) {
+  constexpr int kOwn = 8;
+  unsigned long long ka[kOwn];
+  unsigned kb[kOwn];
+  int hd[kOwn] = {};
+  auto load = [&](int v) {
+    const int g = (lane + 32 * v) * k + hd[v];
+    const bool live = lane + 32 * v < L && hd[v] < k;
+    ka[v] = live ? T.k_ord[g] : 0ull;
+    kb[v] = live ? ~static_cast<unsigned>((T.depth[g] << 16) | g) : 0u;
+  };
+#pragma unroll
+  for (int v = 0; v < kOwn; ++v) load(v);
+  unsigned long long ba = 0;
+  unsigned bb = 0;
+  int bv = 0;
+  auto lane_best = [&]() {                         // a tree over the 8 heads
+    unsigned long long ta[kOwn];
+    unsigned tb[kOwn];
+    int tv[kOwn];
+#pragma unroll
+    for (int v = 0; v < kOwn; ++v) { ta[v] = ka[v]; tb[v] = kb[v]; tv[v] = v; }
+#pragma unroll
+    for (int w = kOwn / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int v = 0; v < w; ++v) {
+        const bool hi = ta[v + w] > ta[v] || (ta[v + w] == ta[v] && tb[v + w] > tb[v]);
+        ta[v] = hi ? ta[v + w] : ta[v];
+        tb[v] = hi ? tb[v + w] : tb[v];
+        tv[v] = hi ? tv[v + w] : tv[v];
+      }
+    ba = ta[0];
+    bb = tb[0];
+    bv = tv[0];
+  };
+  lane_best();
+  for (int p = 0; p < want; ++p) {
+    const unsigned hi = unsigned(ba >> 32), lo = unsigned(ba);
+    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    const bool top = hi == mh && lo == ml;
+    const unsigned mb = __reduce_max_sync(0xffffffffu, top ? bb : 0u);
+    if (lane == 0) sel[p] = int(~mb & 0xffffu);
+    if (top && bb == mb) {                         // unique: the node index is in the key
+#pragma unroll
+      for (int v = 0; v < kOwn; ++v)
+        if (v == bv) {
+          ++hd[v];
+          load(v);
+        }
+      lane_best();
+    }
+  }
+  __syncwarp();
+}
+
+// Beam step in one warp: the best nn of the nact (<= 32) extension lists
+// T[nb + j k .. + k), each in score order, by (score, then generation order),
+// best first into act[].  A merge: lane j holds list j's head; each pick is the
+// largest score image (two 32-bit warp maxima), the lowest lane on ties.
+__device__ __forceinline__ void dart_beam_merge(const DartT& T, int nb, int nact, int k, int nn, int* act,
+                                                int lane) {
+  int h = 0, pick = -1;
+  unsigned long long o = lane < nact ? T.s_ord[nb + lane * k] : 0ull;      // 0: list used up
+  for (int p = 0; p < nn; ++p) {
+    const unsigned hi = unsigned(o >> 32), lo = unsigned(o);
+    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    const unsigned win = __ballot_sync(0xffffffffu, o != 0ull && hi == mh && lo == ml);
+    const int wl = __ffs(win) - 1;
+    const int wh = __shfl_sync(0xffffffffu, h, wl);
+    if (lane == p) pick = nb + wl * k + wh;
+    if (lane == wl) {
+      ++h;
+      o = h < k ? T.s_ord[nb + lane * k + h] : 0ull;
+    }
+  }
+  if (lane < nn) act[lane] = pick;
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuildArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  DartNode* T = reinterpret_cast<DartNode*>(smem);                 // [k + (d - 1) w k]
+  const DartT T = dart_t_layout(smem, a.nodes);                    // [k + (d - 1) w k]
   __shared__ int s_tok[kDartMaxDepth][kDartMaxK];
-  __shared__ double s_lp[kDartMaxDepth][kDartMaxK];
+  __shared__ double s_inc[kDartMaxDepth][kDartMaxK];
   __shared__ int s_active[kDartMaxW];
   __shared__ int s_sel[kDartMaxTheta];
-  __shared__ int s_lbase[kDartMaxTheta + 1], s_lhead[kDartMaxTheta + 1];
-  __shared__ int s_nlist;
+  // the depth-first layout's subtree sizes, parents' selection indices and rows
+  // (first the row merges' survivors, 8 warps x kDartSurvCap keys)
+  __shared__ __align__(16) int s_work[3 * (kDartMaxTheta + 1)];
+  static_assert(sizeof(s_work) >= kDartBuildThreads / 32 * kDartSurvCap * 8, "merge scratch");
+
   const int r = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = a.d, k = a.k, w = a.w;
   if (r == 0 && tid == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
-  // ---- per offset (one warp each): the normaliser in float64 and the top-k of
-  // the tile candidates, with ln(p(v) + eps) of each pick
-  for (int i = warp; i < d; i += kDartBuildThreads / 32) {
-    const size_t row = size_t(r) * d + i;
-    const float2* pt = a.part + row * a.ntile;
-    float M = neg_inf();
-    for (int t = lane; t < a.ntile; t += 32) M = fmaxf(M, pt[t].x);
-    M = warp_max(M);
-    double Z = 0.0;
-    for (int t = lane; t < a.ntile; t += 32)
-      if (pt[t].y > 0.f) Z += double(pt[t].y) * exp2(double(pt[t].x) - double(M));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    const double lse2 = double(M) + log2(Z);                // log2 of sum_v 2^(x_v c2)
-    // k-way merge of the tiles' candidate lists (each in descending order): lane
-    // l owns tiles l, l + 32, l + 64, l + 96 and the head index of each
-    const DartCand* c = a.cand + row * a.ntile * k;
-    int head[kDartMaxTilesPerLane];
-    DartCand hc[kDartMaxTilesPerLane];                       // each owned tile's current head
-#pragma unroll
-    for (int u = 0; u < kDartMaxTilesPerLane; ++u) {
-      head[u] = 0;
-      const int tile = lane + 32 * u;
-      hc[u] = tile < a.ntile ? c[size_t(tile) * k] : DartCand{neg_inf(), 0x7fffffff};
-    }
-    float px = 0.f;                                          // lane t: logit of pick t
-    for (int t = 0; t < k; ++t) {
-      float bv = neg_inf();
-      int bi = 0x7fffffff, bu = -1;
-#pragma unroll
-      for (int u = 0; u < kDartMaxTilesPerLane; ++u) {
-        const DartCand x = hc[u];
-        if (x.i != 0x7fffffff && (x.v > bv || (x.v == bv && x.i < bi))) { bv = x.v; bi = x.i; bu = u; }
-      }
-      const int mine = bi;
-      warp_argmax(bv, bi);                      // all lanes take part
-      if (bi != 0x7fffffff && mine == bi) {     // the owner of the pick advances that tile
-#pragma unroll
-        for (int u = 0; u < kDartMaxTilesPerLane; ++u)
-          if (u == bu) {
-            ++head[u];
-            hc[u] = head[u] < k ? c[size_t(lane + 32 * u) * k + head[u]] : DartCand{neg_inf(), 0x7fffffff};
-          }
-      }
-      if (lane == t) px = bv;
-      if (lane == 0) s_tok[i][t] = bi;
-    }
-    __syncwarp();
-    if (lane < k) {                             // ln(p + eps) of every pick at once
-      const int t = lane;
-      const double lp = s_tok[i][t] == 0x7fffffff ? -INFINITY : (double(px) * a.c2 - lse2) * 0.6931471805599453;
-      s_lp[i][t] = log(exp(lp) + a.eps);
-    }
-  }
+  // ---- per offset i (one warp each): the row's top-k from its tile lists and
+  // eq. (10)'s increment of each pick at depth i + 1, computed once:
+  // (0.9^(i+1) ln(p(v) + eps) + 0.5 ln(1 + eps)) / (i + 2)^0.7
+  unsigned long long* s_mrg = reinterpret_cast<unsigned long long*>(s_work) + warp * kDartSurvCap;
+  for (int i = warp; i < d; i += kDartBuildThreads / 32)
+    dart_row_merge(a.part, a.cand, a.ntile, k, a.c2d, a.ln_eps, r * d + i, s_mrg, lane, [&](int t, int id, double lpv) {
+      s_tok[i][t] = id;
+      s_inc[i][t] = (a.pw[i] * lpv + a.ng) / a.sc[i];
+    });
   __syncthreads();
 
-  __syncthreads();
-  if (warp != 0) return;
-  // Everything below runs in warp 0: the beam and the selection are merges of
-  // lists that are already ordered, so no block barrier is needed.
-  //
   // ---- beam over depths.  T[0 .. k) are the root's children; at depth i >= 2
-  // active path j's k extensions are T[nb + j k .. + k).  A path's extensions
-  // come in the order of its offset's picks, i.e. by non-increasing score, so
-  // the w best of a depth are a w-way merge of those lists (lane j owns list j).
-  const double ng = 0.5 * log(1.0 + a.eps);
-  {
-    const double sc1 = pow(2.0, 0.7);
-    for (int t = lane; t < k; t += 32) {
-      const double sv = (0.9 * s_lp[0][t] + ng) / sc1;
-      DartNode n;
-      n.score = sv;
-      n.s_ord = dart_ord(sv);
-      n.k_ord = n.s_ord;
-      n.parent = -1;
-      n.token = s_tok[0][t];
-      n.depth = 1;
-      n.child0 = -1;
-      T[t] = n;
-    }
+  // active path j's k extensions are T[nb + j k .. + k) (all threads build
+  // them); warp 0 then keeps the w best as the next active paths, in order.
+  for (int t = tid; t < k; t += kDartBuildThreads) {
+    const double sv = s_inc[0][t];
+    T.score[t] = sv;
+    T.s_ord[t] = T.k_ord[t] = dart_ord(sv);
+    T.parent[t] = -1;
+    T.token[t] = s_tok[0][t];
+    T.depth[t] = 1;
+    T.child0[t] = -1;
   }
   int nact = min(w, k);
-  for (int j = lane; j < nact; j += 32) s_active[j] = j;
-  __syncwarp();
   int base = 0, count = k;
+  // depth 1: the root's list, in score order (the picks come in logit order)
+  for (int j = tid; j < nact; j += kDartBuildThreads) s_active[j] = j;
+  __syncthreads();
   for (int i = 2; i <= d; ++i) {
     const int nb = base + count;
-    const double pw = pow(0.9, double(i)), sc = pow(double(i + 1), 0.7);
-    for (int q = lane; q < nact * k; q += 32) {
+    for (int q = tid; q < nact * k; q += kDartBuildThreads) {
       const int j = q / k, t = q - j * k;
-      const DartNode& par = T[s_active[j]];
-      DartNode n;
-      n.score = par.score + (pw * s_lp[i - 1][t] + ng) / sc;
-      n.s_ord = dart_ord(n.score);
-      n.k_ord = n.s_ord < par.k_ord ? n.s_ord : par.k_ord;     // key = min(score, parent key)
-      n.parent = s_active[j];
-      n.token = s_tok[i - 1][t];
-      n.depth = i;
-      n.child0 = -1;
-      T[nb + q] = n;
+      const int par = s_active[j], g = nb + q;
+      const double sc = T.score[par] + s_inc[i - 1][t];
+      const unsigned long long so = dart_ord(sc), pk = T.k_ord[par];
+      T.score[g] = sc;
+      T.s_ord[g] = so;
+      T.k_ord[g] = so < pk ? so : pk;                              // key = min(score, parent key)
+      T.parent[g] = par;
+      T.token[g] = s_tok[i - 1][t];
+      T.depth[g] = i;
+      T.child0[g] = -1;
     }
-    for (int j = lane; j < nact; j += 32) T[s_active[j]].child0 = nb + j * k;
-    __syncwarp();
-    const int nnext = min(w, nact * k);
-    int h = 0;                                                 // lane j: head of list j
-    int pick = -1;
-    for (int p = 0; p < nnext; ++p) {
-      unsigned long long bo = 0;
-      int bg = 0x7fffffff;
-      if (lane < nact && h < k) { bg = nb + lane * k + h; bo = T[bg].s_ord; }
-      unsigned long long wo = bo;
-      int wg = bg;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long oo = __shfl_xor_sync(0xffffffffu, wo, o);
-        const int og = __shfl_xor_sync(0xffffffffu, wg, o);
-        if (oo > wo || (oo == wo && og < wg)) { wo = oo; wg = og; }
-      }
-      if (wg == bg) ++h;                                       // the winning list advances
-      if (lane == p) pick = wg;
+    __syncthreads();
+    for (int j = tid; j < nact; j += kDartBuildThreads) T.child0[s_active[j]] = nb + j * k;
+    const int cnt = nact * k, nnext = min(w, cnt);
+    if (i < d && warp == 0) {
+      __syncwarp();
+      dart_beam_merge(T, nb, nact, k, nnext, s_active, lane);
     }
-    if (lane < nnext) s_active[lane] = pick;               // nnext <= w <= 32: lane p holds pick p
-    __syncwarp();
+    __syncthreads();
     base = nb;
-    count = nact * k;
+    count = cnt;
     nact = nnext;
   }
   const int total = base + count;
-
-  // ---- best-first selection: a merge of the open child lists.  The root's
-  // list is T[0 .. k); a picked node that was extended opens its k children.
-  // Within a list keys do not increase, and across lists the order is (key
-  // desc, depth asc, generation asc), so every pick is the best node left.
   const int want = min(a.theta, total);
-  if (lane == 0) { s_lbase[0] = 0; s_lhead[0] = 0; s_nlist = 1; }
-  __syncwarp();
-  for (int p = 0; p < want; ++p) {
-    const int nl = s_nlist;
-    unsigned long long bk = 0;
-    int bd = 0x7fffffff, bi = 0x7fffffff, bl = -1;
-    for (int l = lane; l < nl; l += 32) {
-      if (s_lhead[l] >= k) continue;
-      const int id = s_lbase[l] + s_lhead[l];
-      const DartNode& n = T[id];
-      if (bl < 0 || dart_better(n.k_ord, n.depth, id, bk, bd, bi)) { bk = n.k_ord; bd = n.depth; bi = id; bl = l; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int od = __shfl_xor_sync(0xffffffffu, bd, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      if (ol >= 0 && (bl < 0 || dart_better(ok, od, oi, bk, bd, bi))) { bk = ok; bd = od; bi = oi; bl = ol; }
-    }
-    if (lane == 0) {
-      s_sel[p] = bi;
-      ++s_lhead[bl];
-      const int c0 = T[bi].child0;
-      if (c0 >= 0) {
-        s_lbase[s_nlist] = c0;
-        s_lhead[s_nlist] = 0;
-        ++s_nlist;
-      }
-    }
-    __syncwarp();
-  }
 
-  // ---- the tree, depth first from the root, children in selection order.
-  // Child lists first (selection order kept), then one walk; T[].depth and
-  // T[].child0 are reused as the next-sibling link and the output row.
-  if (tid == 0) {
-    int32_t* par_out = a.parents + size_t(r) * (a.theta + 1);
-    int32_t* tok_out = a.tokens + size_t(r) * (a.theta + 1);
-    for (int q = 0; q <= a.theta; ++q) { par_out[q] = -1; tok_out[q] = 0; }
-    int root_first = -1, root_last = -1;
-    for (int q = 0; q < want; ++q) {                  // first / last child of each selected node
-      T[s_sel[q]].score = __longlong_as_double(-1ll); // first child (as an int in the bits)
-      T[s_sel[q]].s_ord = ~0ull;                       // last child
-    }
-    for (int q = 0; q < want; ++q) {
-      const int id = s_sel[q];
-      T[id].depth = -1;                               // next sibling
-      const int pa = T[id].parent;
-      if (pa < 0) {
-        if (root_first < 0) root_first = id; else T[root_last].depth = id;
-        root_last = id;
-      } else {
-        const int last = int(static_cast<long long>(T[pa].s_ord));
-        if (last < 0) T[pa].score = __longlong_as_double(id); else T[last].depth = id;
-        T[pa].s_ord = static_cast<unsigned long long>(static_cast<long long>(id));
-      }
-    }
-    int next = 1;
-    int stack[kDartMaxDepth + 1];
-    int sp = -1;
-    for (int id = root_first; id >= 0;) {
-      T[id].child0 = next;
-      const int pa = T[id].parent;
-      par_out[next] = pa < 0 ? 0 : T[pa].child0;
-      tok_out[next] = T[id].token;
-      ++next;
-      const int first = int(__double_as_longlong(T[id].score));
-      if (first >= 0) {                               // descend
-        stack[++sp] = id;
-        id = first;
-        continue;
-      }
-      int sib = T[id].depth;                          // else the next sibling, climbing as needed
-      while (sib < 0 && sp >= 0) sib = T[stack[sp--]].depth;
-      id = sib;
-    }
-    a.n_nodes[r] = next;
+  // ---- selection: the want best nodes of T by (key, then smaller depth, then
+  // generation order), best first.  Keys never increase along a path and ties
+  // go to the shallower node, so this set is ancestor-closed.  T is a run of
+  // lists of k nodes (the root's, then each extended path's extensions), each
+  // already in this order, so the selection is a merge of all of them.
+  if (warp == 0) dart_select_merge(T, total / k, k, want, s_sel, lane);
+  __syncthreads();
+
+  // ---- the tree, depth first from the root, children in selection order:
+  // subtree sizes bottom-up, then each node's row = its parent's row + 1 +
+  // the sizes of its earlier-selected siblings, top-down.  T.child0 now holds
+  // the node's selection index.
+  int* s_sub = s_work;
+  int* s_pq = s_sub + (kDartMaxTheta + 1);
+  int* s_row = s_pq + (kDartMaxTheta + 1);
+  for (int q = tid; q < want; q += kDartBuildThreads) T.child0[s_sel[q]] = q;
+  __syncthreads();
+  for (int q = tid; q < want; q += kDartBuildThreads) {
+    const int pa = T.parent[s_sel[q]];
+    s_pq[q] = pa < 0 ? -1 : T.child0[pa];
+    s_sub[q] = 1;
   }
+  __syncthreads();
+  for (int lev = d; lev >= 2; --lev) {
+    for (int q = tid; q < want; q += kDartBuildThreads)
+      if (T.depth[s_sel[q]] == lev) atomicAdd(&s_sub[s_pq[q]], s_sub[q]);
+    __syncthreads();
+  }
+  // offset of each node below its parent's row: 1 + the sizes of the siblings
+  // selected before it
+  for (int q = tid; q < want; q += kDartBuildThreads) {
+    const int pq = s_pq[q];
+    int before = 1;
+    for (int y = 0; y < q; ++y) before += s_pq[y] == pq ? s_sub[y] : 0;
+    s_row[q] = before;
+  }
+  __syncthreads();
+  for (int lev = 2; lev <= d; ++lev) {           // depth-1 rows are their offsets (root row 0)
+    for (int q = tid; q < want; q += kDartBuildThreads)
+      if (T.depth[s_sel[q]] == lev) s_row[q] += s_row[s_pq[q]];
+    __syncthreads();
+  }
+  int32_t* par_out = a.parents + size_t(r) * (a.theta + 1);
+  int32_t* tok_out = a.tokens + size_t(r) * (a.theta + 1);
+  for (int q = tid; q <= a.theta; q += kDartBuildThreads) {
+    if (q == 0 || q > want) { par_out[q] = -1; tok_out[q] = 0; }
+  }
+  for (int q = tid; q < want; q += kDartBuildThreads) {
+    const int pq = s_pq[q];
+    par_out[s_row[q]] = pq < 0 ? 0 : s_row[pq];
+    tok_out[s_row[q]] = T.token[s_sel[q]];
+  }
+  if (tid == 0) a.n_nodes[r] = want + 1;
 }
 
 }  // namespace specv
@@ -394,7 +699,7 @@ bool dart_plan(int R, int d, long V, int k, int w, int theta, specv_dtype dtype,
   p->vw = dtype == SPECV_BF16 ? 8 : 4;
   const long tile = 32L * kDartVpt * p->vw;
   const long ntile = (V + tile - 1) / tile;
-  if (ntile > 32L * kDartMaxTilesPerLane) return false;
+  if (ntile > kDartMaxTiles) return false;
   p->ntile = int(ntile);
   const size_t rows = size_t(R) * d;
   size_t off = kHeaderBytes;
@@ -404,7 +709,7 @@ bool dart_plan(int R, int d, long V, int k, int w, int theta, specv_dtype dtype,
   off = align256(off + rows * ntile * k * sizeof(DartCand));
   p->total = off;
   const size_t nodes = size_t(k) + size_t(d - 1) * w * k;
-  p->build_smem = nodes * sizeof(DartNode) + (size_t(k) + size_t(theta) * k) * sizeof(int);
+  p->build_smem = nodes * kDartNodeBytes;            // T; the rest is static
   return p->build_smem <= 200 * 1024;
 }
 
@@ -453,23 +758,31 @@ extern "C" specv_status specv_dart_tree(const void* draft_logits, specv_dtype dt
   const long units = long(R) * d * p.ntile;
   const void* tfn = dtype == SPECV_BF16 ? reinterpret_cast<const void*>(&dart_topk_tiles_kernel<uint16_t>)
                                         : reinterpret_cast<const void*>(&dart_topk_tiles_kernel<float>);
+  const size_t tsmem = size_t(kDartTileWarps) * kDartVpt * 32 * 16;       // each warp's tile
   if (cudaLaunchKernel(tfn, dim3(unsigned((units + kDartTileWarps - 1) / kDartTileWarps)), dim3(kDartTileWarps * 32),
-                       targs, 0, st) != cudaSuccess)
+                       targs, tsmem, st) != cudaSuccess)
     return SPECV_ERR_CUDA;
   DartBuildArgs ba;
   ba.part = ta.part;
   ba.cand = ta.cand;
+  ba.ntile = p.ntile;
+  ba.c2d = double(ta.c2);
+  ba.ln_eps = log(kDartEps);
   ba.parents = parents;
   ba.tokens = tokens;
   ba.n_nodes = n_nodes;
   ba.workspace = workspace;
   ba.d = d;
-  ba.ntile = p.ntile;
   ba.k = k;
   ba.w = w;
   ba.theta = theta;
-  ba.c2 = double(ta.c2);
-  ba.eps = kDartEps;
+  ba.nodes = int(size_t(k) + size_t(d - 1) * w * k);
+  // eq. (10)'s constants, from the host's libm (the float64 pipe is narrow)
+  ba.ng = 0.5 * log(1.0 + kDartEps);
+  for (int i = 1; i <= kDartMaxDepth; ++i) {
+    ba.pw[i - 1] = pow(0.9, double(i));
+    ba.sc[i - 1] = pow(double(i + 1), 0.7);
+  }
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&dart_build_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(p.build_smem)) != cudaSuccess)
     return SPECV_ERR_CUDA;

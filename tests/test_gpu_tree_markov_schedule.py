@@ -342,11 +342,46 @@ def _run_dart(lib, logits, dtype, T, k, w, theta):
     (2, 3, 512, 4, 2, 11, "bf16", 0.7),
     (1, 1, 64, 5, 3, 3, "f32", 1.0),
     (2, 5, 1024, 32, 32, 200, "bf16", 1.0),
+    (1, 4, 1024, 16, 8, 300, "f32", 1.0),          # theta > 256: the best-first list merge
 ])
 def test_dart_tree_matches_oracle(lib, R, d, V, k, w, theta, dtype, T):
     logits = synth.make_logits(3.0 * synth.normal(70 + d + k, 1, (R, d, V)), dtype)
     par, tok, nn = _run_dart(lib, logits, dtype, T, k, w, theta)
     ref = oracle.dart_tree(logits.f64, T, k=k, w=w, theta=theta)
+    assert (nn == ref.n_nodes).all()
+    assert (par == ref.parents).all()
+    assert (tok == ref.tokens).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_dart_tree_heavy_ties(lib, dtype):
+    """Integer logits in 0..3: hundreds of values tie at every tile's bound, so
+    the tiles take the repeated-maximum path; equal logits go lower id first."""
+    R, d, V = 2, 3, 151936
+    raw = np.floor(synth.uniform_f32(81, 1, (R, d, V)) * 4.0).astype(np.float64)
+    raw[1, 2, :] = 1.0                                   # one constant row
+    logits = synth.make_logits(raw, dtype)
+    par, tok, nn = _run_dart(lib, logits, dtype, 1.0, 25, 20, 59)
+    ref = oracle.dart_tree(logits.f64, 1.0, k=25, w=20, theta=59)
+    assert (nn == ref.n_nodes).all()
+    assert (par == ref.parents).all()
+    assert (tok == ref.tokens).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_dart_tree_masked_vocabulary(lib, dtype):
+    """Fewer finite logits than k: the rest of the top-k are -inf logits
+    (p = 0), lowest id first, each scored with ln(0 + eps)."""
+    R, d, V, k = 2, 4, 4096, 25
+    raw = np.full((R, d, V), -np.inf)
+    g = synth.normal(82, 1, (R, d, 10))
+    ids = (synth.uniform_u24(82, 2, (R, d, 10)) * V).astype(np.int64)
+    for r in range(R):
+        for i in range(d):
+            raw[r, i, ids[r, i]] = 2.0 * g[r, i]
+    logits = synth.make_logits(raw, dtype)
+    par, tok, nn = _run_dart(lib, logits, dtype, 1.0, k, 6, 40)
+    ref = oracle.dart_tree(logits.f64, 1.0, k=k, w=6, theta=40)
     assert (nn == ref.n_nodes).all()
     assert (par == ref.parents).all()
     assert (tok == ref.tokens).all()
