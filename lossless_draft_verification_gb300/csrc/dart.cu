@@ -20,16 +20,17 @@
 //                    row to finish (a ticket per row) merges the row's tile
 //                    lists the same way and forms ln(p(v) + eps) of the row's
 //                    top-k in float64 from the combined normaliser.
-//   dart_build       one CTA per request: eq. (10)'s increment of every
-//                    (offset, pick) once; all threads extend the active paths,
-//                    one warp keeps the w best (a merge of the score-ordered
-//                    extension lists); the selection is one warp's merge of
-//                    all of T's lists by the key min(score, parent key), then
-//                    smaller depth, then generation order -- keys never
-//                    increase along a path and equal keys go to the shallower
-//                    node, so the theta best are ancestor-closed; the tree's
-//                    depth-first rows (children in selection order) come from
-//                    subtree sizes, one barrier per depth.
+//   dart_build       one CTA per request: warp i merges offset i's tile lists
+//                    into its top-k and eq. (10)'s increments; all threads
+//                    extend the active paths and one warp keeps the w best (a
+//                    merge of the score-ordered extension lists); the
+//                    selection is a block-wide radix select of the theta
+//                    largest keys min(score, parent key), then smaller depth,
+//                    then generation order -- keys never increase along a path
+//                    and equal keys go to the shallower node, so the theta best
+//                    are ancestor-closed; the tree's depth-first rows
+//                    (children in selection order) come from subtree sizes,
+//                    one barrier per depth.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -552,6 +553,104 @@ __device__ __forceinline__ void dart_beam_merge(const DartT& T, int nb, int nact
   __syncwarp();
 }
 
+constexpr int kDartRsCand = 768;          // radix select: candidates ranked at the end
+constexpr int kDartRsBin = 48;            // passes go on while the bin holds more nodes
+
+struct DartRsShared {
+  unsigned long long orw[kDartBuildThreads / 32];
+  int hist[256];
+  unsigned long long ca[kDartRsCand];
+  unsigned cb[kDartRsCand];
+  int dig, above, bsize, nc;
+};
+
+// Block-wide selection of the want best of nodes [lo, lo + n) by (A[g]
+// descending, then B(g) descending; B(g) = ~(depth << 16 | g), so unique),
+// the node indices best first into out[]:
+// 8-bit radix passes over A, from the highest bit in which the nodes differ,
+// narrow the bin that holds the want-th key; the
+// nodes above that bin and the bin's own nodes (at most 256) are then ranked
+// by counting.  Returns false (nothing written) if a bin of more than 256
+// nodes shares all of A, or want + 256 > kDartRsCand.
+template <typename BKey>
+__device__ __forceinline__ bool dart_radix_select(const unsigned long long* A, BKey B, int lo, int n, int want,
+                                                  int* out, DartRsShared& sh, int tid) {
+  if (want + 256 > kDartRsCand) return false;
+  const int warp = tid >> 5, lane = tid & 31;
+  unsigned long long prefix = 0, pmask = 0;
+  int need = want, bsize = n;
+  int shift = 56;
+  if (n > 256) {                                        // bits above the highest differing one are common
+    const unsigned long long ref = A[lo];
+    unsigned long long x = 0;
+    for (int g = lo + tid; g < lo + n; g += kDartBuildThreads) x |= A[g] ^ ref;
+    const unsigned xh = __reduce_or_sync(0xffffffffu, unsigned(x >> 32));
+    const unsigned xl = __reduce_or_sync(0xffffffffu, unsigned(x));
+    if (lane == 0) sh.orw[warp] = (static_cast<unsigned long long>(xh) << 32) | xl;
+    __syncthreads();
+    x = 0;
+#pragma unroll
+    for (int v = 0; v < kDartBuildThreads / 32; ++v) x |= sh.orw[v];
+    if (x == 0) return false;                           // more than 256 nodes share A
+    shift = 63 - __clzll(static_cast<long long>(x)) - 7;                // digit = the 8 bits below it
+  }
+  for (; shift > -8 && bsize > kDartRsBin; shift -= 8) {
+    const unsigned long long dmask = shift >= 0 ? 255ull << shift : 255ull >> -shift;
+    sh.hist[tid] = 0;                                   // 256 threads, 256 bins
+    __syncthreads();
+    for (int g = lo + tid; g < lo + n; g += kDartBuildThreads) {
+      const unsigned long long a = A[g];
+      if ((a & pmask) == prefix)
+        atomicAdd(&sh.hist[shift >= 0 ? (a >> shift) & 255u : (a << -shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {                                    // lane l: bins 255 - 8l .. 248 - 8l
+      int c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = sh.hist[255 - 8 * lane - j]; tot += c[j]; }
+      int dummy;
+      int run = warp_excl_scan(tot, lane, &dummy);
+      int found = -1, above = 0, bs = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (found < 0 && run < need && run + c[j] >= need) { found = 255 - 8 * lane - j; above = run; bs = c[j]; }
+        run += c[j];
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, found >= 0);
+      if (lane == __ffs(m) - 1) { sh.dig = found; sh.above = above; sh.bsize = bs; }
+    }
+    __syncthreads();
+    need -= sh.above;
+    bsize = sh.bsize;
+    const unsigned long long dg = static_cast<unsigned long long>(sh.dig);
+    prefix |= shift >= 0 ? dg << shift : dg >> -shift;
+    pmask |= dmask;
+  }
+  if (bsize > 256) return false;
+  // gather the nodes above the bin (want - need of them) and the bin's nodes
+  if (tid == 0) sh.nc = 0;
+  __syncthreads();
+  for (int g = lo + tid; g < lo + n; g += kDartBuildThreads) {
+    const unsigned long long a = A[g];
+    if ((a & pmask) >= prefix) {
+      const int at = atomicAdd(&sh.nc, 1);
+      sh.ca[at] = a;
+      sh.cb[at] = B(g);
+    }
+  }
+  __syncthreads();
+  const int nc = sh.nc;
+  for (int x = tid; x < nc; x += kDartBuildThreads) {
+    const unsigned long long xa = sh.ca[x];
+    const unsigned xb = sh.cb[x];
+    int rk = 0;
+    for (int y = 0; y < nc; ++y) rk += (sh.ca[y] > xa || (sh.ca[y] == xa && sh.cb[y] > xb)) ? 1 : 0;
+    if (rk < want) out[rk] = int(~xb & 0xffffu);
+  }
+  __syncthreads();
+  return true;
+}
+
 __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuildArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const DartT T = dart_t_layout(smem, a.nodes);                    // [k + (d - 1) w k]
@@ -564,9 +663,13 @@ __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuild
   __shared__ __align__(16) int s_work[3 * (kDartMaxTheta + 1)];
   static_assert(sizeof(s_work) >= kDartBuildThreads / 32 * kDartSurvCap * 8, "merge scratch");
 
+  DartRsShared& rs = *reinterpret_cast<DartRsShared*>(s_work);                  // by phase
+  static_assert(sizeof(s_work) >= sizeof(DartRsShared), "radix select scratch");
   const int r = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d = a.d, k = a.k, w = a.w;
+  // the selection's second sort key: smaller depth, then older
+  auto bkey = [&](int g) { return ~static_cast<unsigned>((T.depth[g] << 16) | g); };
   if (r == 0 && tid == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
   // ---- per offset i (one warp each): the row's top-k from its tile lists and
@@ -615,10 +718,7 @@ __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuild
     __syncthreads();
     for (int j = tid; j < nact; j += kDartBuildThreads) T.child0[s_active[j]] = nb + j * k;
     const int cnt = nact * k, nnext = min(w, cnt);
-    if (i < d && warp == 0) {
-      __syncwarp();
-      dart_beam_merge(T, nb, nact, k, nnext, s_active, lane);
-    }
+    if (i < d && warp == 0) dart_beam_merge(T, nb, nact, k, nnext, s_active, lane);
     __syncthreads();
     base = nb;
     count = cnt;
@@ -632,7 +732,8 @@ __global__ void __launch_bounds__(kDartBuildThreads) dart_build_kernel(DartBuild
   // go to the shallower node, so this set is ancestor-closed.  T is a run of
   // lists of k nodes (the root's, then each extended path's extensions), each
   // already in this order, so the selection is a merge of all of them.
-  if (warp == 0) dart_select_merge(T, total / k, k, want, s_sel, lane);
+  if (!dart_radix_select(T.k_ord, bkey, 0, total, want, s_sel, rs, tid) && warp == 0)
+    dart_select_merge(T, total / k, k, want, s_sel, lane);
   __syncthreads();
 
   // ---- the tree, depth first from the root, children in selection order:

@@ -342,7 +342,8 @@ def _run_dart(lib, logits, dtype, T, k, w, theta):
     (2, 3, 512, 4, 2, 11, "bf16", 0.7),
     (1, 1, 64, 5, 3, 3, "f32", 1.0),
     (2, 5, 1024, 32, 32, 200, "bf16", 1.0),
-    (1, 4, 1024, 16, 8, 300, "f32", 1.0),          # theta > 256: the best-first list merge
+    (1, 4, 1024, 16, 8, 300, "f32", 1.0),
+    (1, 4, 1024, 32, 8, 600, "bf16", 1.0),         # theta > 512: the selection's list merge
 ])
 def test_dart_tree_matches_oracle(lib, R, d, V, k, w, theta, dtype, T):
     logits = synth.make_logits(3.0 * synth.normal(70 + d + k, 1, (R, d, V)), dtype)
@@ -356,7 +357,9 @@ def test_dart_tree_matches_oracle(lib, R, d, V, k, w, theta, dtype, T):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_dart_tree_heavy_ties(lib, dtype):
     """Integer logits in 0..3: hundreds of values tie at every tile's bound, so
-    the tiles take the repeated-maximum path; equal logits go lower id first."""
+    the tiles take the repeated-maximum path; equal logits go lower id first.
+    Whole depths of equal scores send the beam and the selection to their list
+    merges."""
     R, d, V = 2, 3, 151936
     raw = np.floor(synth.uniform_f32(81, 1, (R, d, V)) * 4.0).astype(np.float64)
     raw[1, 2, :] = 1.0                                   # one constant row
