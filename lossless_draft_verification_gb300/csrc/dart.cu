@@ -150,17 +150,19 @@ __device__ __forceinline__ DartCand dart_unkey16(uint32_t key, int tile_base) {
   return DartCand{__uint_as_float(h << 16), tile_base + int(0xffffu - (key & 0xffffu))};
 }
 
-// the k-th largest (1 <= k <= 32) of the warp's 32 values, equal values
-// counted once per lane
+// the k-th largest (1 <= k <= 32) of the warp's 32 values (not NaN), equal
+// values counted once per lane: a bitonic sort across the lanes, descending
 __device__ __forceinline__ float warp_kth_largest_f(float v, int k, int lane) {
-  int rank = 0;
 #pragma unroll
-  for (int l = 0; l < 32; ++l) {
-    const float o = __shfl_sync(0xffffffffu, v, l);
-    rank += (o > v || (o == v && l < lane)) ? 1 : 0;
-  }
-  const unsigned m = __ballot_sync(0xffffffffu, rank == k - 1);
-  return __shfl_sync(0xffffffffu, v, __ffs(m) - 1);
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool desc = (lane & size) == 0 || size == 32;   // this run's direction
+      const bool low = (lane & stride) == 0;                  // the lower lane of the pair
+      v = (low == desc) ? fmaxf(v, o) : fminf(v, o);
+    }
+  return __shfl_sync(0xffffffffu, v, k - 1);
 }
 
 // One warp merges a row's tile results: the combined normaliser and the top-k
@@ -278,7 +280,7 @@ __device__ __forceinline__ __nv_bfloat162 dart_as_b2(uint32_t u) {
 }
 
 template <typename Elem>
-__global__ void __launch_bounds__(kDartTileWarps * 32, 2) dart_topk_tiles_kernel(DartTileArgs a) {
+__global__ void __launch_bounds__(kDartTileWarps * 32, 3) dart_topk_tiles_kernel(DartTileArgs a) {
   using S = Slot<Elem, true>;
   constexpr int VW = S::VW;
   constexpr int NE = kDartVpt * VW;                          // elements per lane
@@ -860,6 +862,8 @@ extern "C" specv_status specv_dart_tree(const void* draft_logits, specv_dtype dt
   const void* tfn = dtype == SPECV_BF16 ? reinterpret_cast<const void*>(&dart_topk_tiles_kernel<uint16_t>)
                                         : reinterpret_cast<const void*>(&dart_topk_tiles_kernel<float>);
   const size_t tsmem = size_t(kDartTileWarps) * kDartVpt * 32 * 16;       // each warp's tile
+  if (cudaFuncSetAttribute(tfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return SPECV_ERR_CUDA;                                                  // three 48 KB CTAs per SM
   if (cudaLaunchKernel(tfn, dim3(unsigned((units + kDartTileWarps - 1) / kDartTileWarps)), dim3(kDartTileWarps * 32),
                        targs, tsmem, st) != cudaSuccess)
     return SPECV_ERR_CUDA;
