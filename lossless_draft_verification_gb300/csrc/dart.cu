@@ -13,15 +13,15 @@
 //                    logits, in the only pass over them (HBM-bound): the
 //                    tile's softmax partial (max * c2, sum of 2^(x c2 - max c2))
 //                    and its top-k (logit, id) candidates, lowest id first
-//                    among equal logits.  The k-th best of the 32 lanes' own
-//                    best elements bounds the tile's k-th best from below, so
-//                    only the few values at or above it are compacted to
-//                    shared memory and ranked by counting.  The last warp of a
-//                    row to finish (a ticket per row) merges the row's tile
-//                    lists the same way and forms ln(p(v) + eps) of the row's
-//                    top-k in float64 from the combined normaliser.
+//                    among equal logits.  The k-th largest of the 32 lane
+//                    maxima comes from k distinct elements, so it bounds the
+//                    tile's k-th best from below: only the few values at or
+//                    above it are compacted to shared memory and ranked by
+//                    counting.
 //   dart_build       one CTA per request: warp i merges offset i's tile lists
-//                    into its top-k and eq. (10)'s increments; all threads
+//                    into the row's top-k (the same bound, from the lists'
+//                    heads), ln(p(v) + eps) from the combined normaliser and
+//                    eq. (10)'s increments; all threads
 //                    extend the active paths and one warp keeps the w best (a
 //                    merge of the score-ordered extension lists); the
 //                    selection is a block-wide radix select of the theta
