@@ -242,6 +242,43 @@ def test_dart_tree_without_pruning_is_the_brute_force_selection():
     np.testing.assert_allclose(sorted(t.key[0, 1:], reverse=True), [b[0] for b in best], rtol=1e-12)
 
 
+def test_dart_tree_masked_vocabulary_is_the_brute_force_selection():
+    """Two finite logits per offset and k = 3: each offset's third pick is the
+    lowest-id token of probability 0, scored with ln(0 + eps).  No path is
+    dropped (w = k^d), so the tree is again the theta largest bottleneck keys
+    over every path, enumerated here."""
+    rng = np.random.default_rng(64)
+    d, V, k, theta = 3, 9, 3, 12
+    x = np.full((1, d, V), -np.inf)
+    for i in range(d):
+        ids = rng.choice(V, size=2, replace=False)
+        x[0, i, ids] = rng.normal(size=2) * 2.0
+    t = oracle.dart_tree(x, 1.0, k=k, w=k ** d, theta=theta)
+    p = scipy.special.softmax(x[0], axis=-1)
+    assert (p > 0).sum() == 2 * d
+    tops = [list(np.argsort(-p[i], kind="stable")[:k]) for i in range(d)]
+    paths = []
+    for depth in range(1, d + 1):
+        for combo in itertools.product(*tops[:depth]):
+            s_, key = 0.0, np.inf
+            for i, v in enumerate(combo, start=1):
+                s_ += _delta(p, i, v)
+                key = min(key, s_)
+            paths.append((key, depth, combo))
+    best = sorted(paths, key=lambda e: (-e[0], e[1]))
+    assert (best[theta - 1][0], best[theta - 1][1]) != (best[theta][0], best[theta][1])   # no tie at the cut
+    got = []
+    for i in range(1, t.n_nodes[0]):
+        toks, j = [], i
+        while j > 0:
+            toks.append(int(t.tokens[0, j]))
+            j = int(t.parents[0, j])
+        got.append(tuple(reversed(toks)))
+    assert sorted(got) == sorted(tuple(int(v) for v in c) for _, _, c in best[:theta])
+    for i in range(d):                                    # the masked pick is the lowest zero-probability id
+        assert tops[i][2] == int(np.flatnonzero(p[i] == 0)[0])
+
+
 def test_dart_tree_beam_of_one_is_the_argmax_chain_with_its_siblings():
     rng = np.random.default_rng(62)
     d, V, k = 4, 20, 3
