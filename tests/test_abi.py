@@ -83,3 +83,56 @@ def test_invalid_arguments_rejected_before_launch():
     assert specv.specv_markov_draft(fake, fake, fake, fake, fake, 2, 3, 10, 20, 1.0, fake, None, 0, fake, 1 << 30, None) == E
     assert specv.specv_schedule(fake, fake, 5, 3, 4, fake, None, fake, 256, None) == E   # R > B_max
     assert specv.specv_schedule(fake, fake, 5000, 3, 8192, fake, None, fake, 256, None) == E
+
+
+def test_next_rows_reject_invalid_arguments_before_launch():
+    """The scheduler's global form, the pruning, the confidence head and the
+    DART tree validate on the host: every call below returns before any CUDA
+    call (R == 0 is a no-op)."""
+    import lossless_draft_verification_gb300 as specv
+    E, U = specv.SPECV_ERR_INVALID_ARG, specv.SPECV_ERR_UNSUPPORTED
+    fake = 1 << 20                          # 256-byte aligned, never dereferenced
+    # global-search scheduler: R > B_max, missing SPS table, short workspace
+    assert specv.specv_schedule_global(fake, fake, fake, 5, 3, 4, fake, None, fake, 256, None) == E
+    assert specv.specv_schedule_global(fake, fake, None, 2, 3, 8, fake, None, fake, 256, None) == E
+    assert specv.specv_schedule_global(fake, fake, fake, 2, 3, 8, fake, None, fake, 16, None) == E
+    assert specv.specv_schedule_global(None, None, None, 0, 3, 8, None, None, None, 0, None) == 0
+    # pruning: NaN threshold, misaligned confidences, R == 0
+    assert specv.specv_prune_threshold(fake, 2, 3, float("nan"), fake, fake, 256, None) == E
+    assert specv.specv_prune_threshold(fake + 2, 2, 3, 0.5, fake, fake, 256, None) == E
+    assert specv.specv_prune_threshold(None, 0, 3, 0.5, None, None, 0, None) == 0
+    # confidence head: NaN bias, negative gamma, missing anchor, short workspace
+    ch = specv.specv_confidence_head
+    assert ch(fake, fake, fake, float("nan"), fake, fake, 2, 3, 64, 100, 16, fake, fake, 256, None) == E
+    assert ch(fake, fake, fake, 0.5, fake, fake, 2, -1, 64, 100, 16, fake, fake, 256, None) == E
+    assert ch(fake, fake, fake, 0.5, None, fake, 2, 3, 64, 100, 16, fake, fake, 256, None) == E
+    assert ch(fake, fake, fake, 0.5, fake, fake, 2, 3, 64, 100, 16, fake, fake, 8, None) == E
+    assert ch(None, None, None, 0.5, None, None, 0, 3, 64, 100, 16, None, None, 0, None) == 0
+    assert specv.specv_confidence_head_workspace_size(512, 7) == 256
+    # DART tree: ranges of d, k, w, theta, dtype and T; unaligned rows and
+    # shapes past the tile or shared-memory limits are unsupported
+    ws = specv.specv_dart_tree_workspace_size
+    BF, F32 = specv.SPECV_BF16, specv.SPECV_F32
+    assert ws(16, 8, 151936, 25, 20, 59, BF) > 16 * 8 * 60 * 25 * 8
+    assert ws(16, 9, 151936, 25, 20, 59, BF) == 0          # d > 8
+    assert ws(16, 8, 151936, 33, 20, 59, BF) == 0          # k > 32
+    assert ws(16, 8, 20, 25, 20, 59, BF) == 0              # k > V
+    assert ws(16, 8, 151936, 25, 20, 1024, BF) == 0        # theta > 1023
+    assert ws(16, 8, 151936, 32, 32, 59, BF) == 0          # 7200 nodes: over 200 KB of shared memory
+    assert ws(16, 8, 128 * 2560 + 8, 25, 20, 59, BF) == 0  # more than 128 warp tiles per row
+    assert ws(16, 8, 151936, 25, 20, 59, 7) == 0           # dtype
+    dt = specv.specv_dart_tree
+    args = lambda x, dtype, V, T, k, w, th, nb: (x, dtype, 2, 3, V, T, k, w, th, fake, fake, fake, fake, nb, None)
+    nb = ws(2, 3, 4096, 4, 2, 11, BF)
+    assert nb > 0
+    assert dt(*args(fake, BF, 4096, 1.0, 0, 2, 11, nb)) == E                 # k < 1
+    assert dt(fake, BF, 2, 0, 4096, 1.0, 4, 2, 11, fake, fake, fake, fake, nb, None) == E   # d < 1
+    assert dt(*args(fake, BF, 4096, 0.0, 4, 2, 11, nb)) == E                 # T <= 0
+    assert dt(*args(fake, BF, 4096, float("nan"), 4, 2, 11, nb)) == E
+    assert dt(*args(fake, BF, 4096, 1.0, 4, 0, 11, nb)) == E                 # w < 1
+    assert dt(*args(fake, BF, 4096, 1.0, 4, 2, 0, nb)) == E                  # theta < 1
+    assert dt(*args(fake + 8, BF, 4096, 1.0, 4, 2, 11, nb)) == U             # rows not 16-byte aligned
+    assert dt(*args(fake, BF, 4100, 1.0, 4, 2, 11, nb)) == U                 # V not a multiple of 8 (bf16)
+    assert dt(*args(fake, F32, 4098, 1.0, 4, 2, 11, nb)) == U                # V not a multiple of 4 (float32)
+    assert dt(*args(fake, BF, 4096, 1.0, 4, 2, 11, nb - 256)) == E           # short workspace
+    assert dt(None, BF, 0, 3, 4096, 1.0, 4, 2, 11, None, None, None, None, 0, None) == 0
