@@ -31,7 +31,8 @@ __all__ = [
     "specv_read_device_error",
     "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
     "specv_shard_argmax_combine",
-    "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "read_device_error",
+    "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "schedule_global",
+    "prune_threshold", "confidence_head", "dart_tree", "read_device_error",
 ]
 
 (SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_DEVICE_DATA, SPECV_ERR_TIMEOUT,
@@ -403,6 +404,90 @@ def schedule(conf, sps, B_max: int | None = None, workspace=None, stream=None):
                         _stream_ptr(stream))
     _raise(st, "specv_schedule")
     return lengths, theta
+
+
+def schedule_global(conf, sps, conf_stale=None, B_max: int | None = None, workspace=None, stream=None):
+    """Asynchronous global-search scheduler: the count K from conf_stale (or
+    conf when None), no early stop; the entries from conf.  conf and conf_stale
+    [R, gamma] float32, sps [B_max] float64.  Returns (lengths [R] int32,
+    theta_best [1] float64)."""
+    torch = _torch()
+    R, gamma = conf.shape
+    dev = conf.device
+    _check(conf, "conf", dev, torch.float32)
+    _check(conf_stale, "conf_stale", dev, torch.float32, (R, gamma))
+    _check(sps, "sps", dev, torch.float64)
+    B_max = sps.shape[0] if B_max is None else B_max
+    lengths = torch.empty(R, dtype=torch.int32, device=dev)
+    theta = torch.empty(1, dtype=torch.float64, device=dev)
+    nbytes = specv_schedule_workspace_size(R, gamma)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_schedule_global(_p(conf), _p(conf_stale), _p(sps), R, gamma, int(B_max), _p(lengths), _p(theta),
+                               _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_schedule_global")
+    return lengths, theta
+
+
+def prune_threshold(conf, threshold: float, workspace=None, stream=None):
+    """Confidence-threshold suffix pruning; conf [R, gamma] float32.  Returns
+    lengths [R] int32: the leading positions whose running product of
+    confidences stays >= threshold."""
+    torch = _torch()
+    R, gamma = conf.shape
+    dev = conf.device
+    _check(conf, "conf", dev, torch.float32)
+    lengths = torch.empty(R, dtype=torch.int32, device=dev)
+    nbytes = specv_schedule_workspace_size(R, gamma)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_prune_threshold(_p(conf), R, gamma, float(threshold), _p(lengths), _p(ws), ws.numel(),
+                               _stream_ptr(stream))
+    _raise(st, "specv_prune_threshold")
+    return lengths
+
+
+def confidence_head(h, W1, w, b: float, anchor, draft_tokens, workspace=None, stream=None):
+    """DSpark's confidence head: h [R, gamma, H] bf16, W1 [V, rank] bf16,
+    w [H + rank] float32, anchor [R] and draft_tokens [R, gamma] int32.
+    Returns conf [R, gamma] float32."""
+    torch = _torch()
+    R, gamma, H = h.shape
+    V, rank = W1.shape
+    dev = h.device
+    _check(h, "h", dev, torch.bfloat16)
+    _check(W1, "W1", dev, torch.bfloat16)
+    _check(w, "w", dev, torch.float32, (H + rank,))
+    _check(anchor, "anchor", dev, torch.int32, (R,))
+    _check(draft_tokens, "draft_tokens", dev, torch.int32, (R, gamma))
+    conf = torch.empty(R, gamma, dtype=torch.float32, device=dev)
+    nbytes = specv_confidence_head_workspace_size(R, gamma)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_confidence_head(_p(h), _p(W1), _p(w), float(b), _p(anchor), _p(draft_tokens), R, gamma, H, V, rank,
+                               _p(conf), _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_confidence_head")
+    return conf
+
+
+def dart_tree(draft_logits, temperature: float = 1.0, k: int = 25, w: int = 20, theta: int = 59, workspace=None,
+              stream=None):
+    """DART's candidate tree without the n-gram index; draft_logits [R, d, V]
+    bfloat16 or float32.  Returns (parents, tokens [R, theta + 1] int32,
+    n_nodes [R] int32): row 0 is the root, rows are in depth-first order."""
+    torch = _torch()
+    R, d, V = draft_logits.shape
+    dev = draft_logits.device
+    _check(draft_logits, "draft_logits", dev)
+    dt = _dtype_code(draft_logits)
+    parents = torch.empty(R, theta + 1, dtype=torch.int32, device=dev)
+    tokens = torch.empty(R, theta + 1, dtype=torch.int32, device=dev)
+    n_nodes = torch.empty(R, dtype=torch.int32, device=dev)
+    nbytes = specv_dart_tree_workspace_size(R, d, V, k, w, theta, dt)
+    if nbytes == 0:
+        raise SpecvError(SPECV_ERR_UNSUPPORTED, "specv_dart_tree_workspace_size")
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_dart_tree(_p(draft_logits), dt, R, d, V, float(temperature), k, w, theta, _p(parents), _p(tokens),
+                         _p(n_nodes), _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_dart_tree")
+    return parents, tokens, n_nodes
 
 
 def read_device_error(workspace, stream=None) -> int:

@@ -136,3 +136,31 @@ def test_next_rows_reject_invalid_arguments_before_launch():
     assert dt(*args(fake, F32, 4098, 1.0, 4, 2, 11, nb)) == U                # V not a multiple of 4 (float32)
     assert dt(*args(fake, BF, 4096, 1.0, 4, 2, 11, nb - 256)) == E           # short workspace
     assert dt(None, BF, 0, 3, 4096, 1.0, 4, 2, 11, None, None, None, None, 0, None) == 0
+
+
+def test_tensor_helpers_check_shapes_before_any_device_call():
+    """The helpers of the newer entry points reject mismatched tensors (and the
+    DART helper unsupported shapes) before they touch a stream or a device."""
+    import torch
+    import lossless_draft_verification_gb300 as specv
+    conf = torch.zeros(4, 7, dtype=torch.float32)
+    sps = torch.ones(64, dtype=torch.float64)
+    with pytest.raises(ValueError):
+        specv.schedule_global(conf, sps, conf_stale=torch.zeros(4, 6, dtype=torch.float32))
+    with pytest.raises(TypeError):
+        specv.schedule_global(conf, sps.float())
+    with pytest.raises(TypeError):
+        specv.prune_threshold(conf.double(), 0.5)
+    h = torch.zeros(4, 7, 64, dtype=torch.bfloat16)
+    W1 = torch.zeros(100, 16, dtype=torch.bfloat16)
+    anchor = torch.zeros(4, dtype=torch.int32)
+    toks = torch.zeros(4, 7, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        specv.confidence_head(h, W1, torch.zeros(64, dtype=torch.float32), 0.5, anchor, toks)    # w is H + rank long
+    with pytest.raises(TypeError):
+        specv.confidence_head(h.float(), W1, torch.zeros(80, dtype=torch.float32), 0.5, anchor, toks)
+    with pytest.raises(TypeError):
+        specv.dart_tree(torch.zeros(2, 3, 64, dtype=torch.float16))
+    with pytest.raises(specv.SpecvError):
+        specv.dart_tree(torch.zeros(2, 9, 4096, dtype=torch.bfloat16))                     # d > 8
+    assert callable(specv.dart_tree) and "dart_tree" in specv.__all__
