@@ -504,7 +504,8 @@ def run_workload(args):
         algo = Rt * dt_ * Vt * 2
         units, unit, metric = Rt, "trees/s", "DART candidate-tree construction: trees/sec"
         desc, launches, kernel = ("DART tree: R=16, d=8 offsets, V=151936 bf16, top-25, beam 20, 59 nodes", 2,
-                                  "dart_topk_tiles + dart_build")
+                                  "whole specv_dart_tree call: dart_topk_tiles reads the logits once (HBM); "
+                                  "dart_build, about 70 % of the call, is per-request latency")
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                 "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
     elif w == "confidence":
