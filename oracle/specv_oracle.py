@@ -28,7 +28,7 @@ Notation follows the DART notes: q = target distribution, p = draft
 distribution.  Probabilities are float64; bf16/float32 logits are widened to
 float64 exactly by the caller.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent, ambiguous or garbled:
   R1  temperature: q = softmax(target / T), p = softmax(draft / T); T = 0 means
       greedy (argmax) verification.
   R2  accept iff u < min(1, q(x)/p(x)) with u in [0, 1); p(x) = 0 accepts.
