@@ -290,6 +290,75 @@ def test_greedy_lengths_and_cstar():
     assert np.isnan(cst[0]).all() and np.isnan(cst[1, 2:]).all() and not np.isnan(cst[2]).any()
 
 
+def _cstar_case():
+    """Hand case for c* at T = 0 (reading R7): 2 requests, gamma = 4, V = 5.
+    Each row is -1 except the entries listed; argmaxes are read off by eye."""
+    R, gamma, V = 2, 4, 5
+    t = np.full((R, gamma + 1, V), -1.0)
+    d = np.full((R, gamma, V), -1.0)
+    # request 0: target argmaxes 2, 4, 1, 3, 0 for rows 0..4
+    for k, g in enumerate([2, 4, 1, 3, 0]):
+        t[0, k, g] = 2.0
+    # draft argmaxes 2 (agrees), 3 (disagrees; equals target row 3's argmax, so
+    # comparing draft row k with target row k+1 would score it), tie {1, 3} with
+    # target 1 (agrees: lowest id), 0 (disagrees; equals target row 4's argmax)
+    d[0, 0, 2] = 1.5
+    d[0, 1, 3] = 0.5
+    d[0, 2, 1] = 0.7
+    d[0, 2, 3] = 0.7
+    d[0, 3, 0] = 3.0
+    # request 1: target argmaxes 0, 0, 3, 3, 2; draft: tie {1, 3} with target 3
+    # (disagrees: the draft's argmax is 1), 0 (agrees), 3 (agrees), 4 (disagrees)
+    for k, g in enumerate([0, 0, 3, 3, 2]):
+        t[1, k, g] = 1.0
+    t[1, 2, 4] = 0.5
+    d[1, 0, 1] = 2.0
+    d[1, 0, 3] = 2.0
+    d[1, 1, 0] = 0.1
+    d[1, 2, 3] = 5.0
+    d[1, 3, 4] = 1.0
+    want = np.array([[1.0, 0.0, 1.0, 0.0], [0.0, 1.0, 1.0, 0.0]])
+    return t, d, want
+
+
+def test_cstar_at_T0_hand_case():
+    """c* at T = 0 is the indicator that the draft's and the target's argmaxes
+    at the same position agree, ties to the lowest id (reading R7).  Literal
+    expected values; a slip to target row k+1, or a reduction over the
+    position axis, changes at least one entry."""
+    t, d, want = _cstar_case()
+    got = oracle.tv_accept(t, d, 0.0)
+    assert got.shape == want.shape and (got == want).all()
+    x = np.zeros((2, 4), dtype=np.int64)
+    ell = np.array([4, 3])
+    _, _, cst, _ = oracle.verify_chain_greedy(t, x, ell, d)
+    assert (cst[0] == want[0]).all()
+    assert (cst[1, :3] == want[1, :3]).all() and np.isnan(cst[1, 3])
+
+
+def test_cstar_at_T0_is_the_small_T_limit():
+    """Away from ties, c*(T) = sum_v min(p_T, q_T) tends to the argmax
+    indicator as T -> 0+ (the limit reading R7 takes): with logit gaps >= 0.5,
+    T = 1e-3 already puts less than e^-400 of each row's mass off its argmax."""
+    t, d, want = _cstar_case()
+    lim = oracle.tv_accept_probs(scipy.special.softmax(t[:, :4] / 1e-3, axis=-1),
+                                 scipy.special.softmax(d / 1e-3, axis=-1))
+    no_tie = np.ones_like(want, dtype=bool)
+    no_tie[0, 2] = no_tie[1, 0] = False            # draft ties: the limit there is 1/2 and 0
+    np.testing.assert_allclose(lim[no_tie], want[no_tie], atol=1e-12)
+    np.testing.assert_allclose(lim[~no_tie], [0.5, 0.0], atol=1e-12)
+    # and a random case with distinct maxima, through the oracle's T = 0 branch
+    tr = synth.normal(25, 1, (5, 4, 9))
+    dr = synth.normal(25, 2, (5, 3, 9))
+    dr[::2] = tr[::2, :3] + 0.01 * dr[::2]         # half the requests agree at most positions
+    gap_ok = (np.diff(np.sort(tr, -1)[..., -2:], axis=-1)[..., 0] > 0.05)[:, :3] & \
+             (np.diff(np.sort(dr, -1)[..., -2:], axis=-1)[..., 0] > 0.05)
+    small = oracle.tv_accept(tr, dr, 1e-4)
+    exact = oracle.tv_accept(tr, dr, 0.0)
+    assert gap_ok.sum() >= 8 and 0 < exact[gap_ok].sum() < gap_ok.sum()
+    np.testing.assert_allclose(small[gap_ok], exact[gap_ok], atol=1e-9)
+
+
 def test_T_to_zero_reduces_to_argmax():
     """q replaced by one-hot(argmax target) gives the greedy result for any p
     with full support (SD survey §1.3)."""
