@@ -14,6 +14,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_terminal_summary(terminalreporter):
+    """Print the flagged-threshold counts the parity tests recorded: decisions
+    the GPU took differently from the oracle because the uniform lay within
+    1e-5 of the threshold (allowed, but counted and reported)."""
+    parity = sys.modules.get("parity")
+    if parity is None or not getattr(parity, "REPORT", None):
+        return
+    terminalreporter.write_sep("-", "parity: exact and flagged-threshold counts")
+    for name, counts in parity.REPORT:
+        terminalreporter.write_line(f"{name}: " + ", ".join(f"{k} {v}" for k, v in counts.items()))
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")

@@ -17,6 +17,16 @@ import oracle
 
 TOL = 1e-5
 
+# (test name, counts) of every parity check that counted flagged cases; the
+# session's terminal summary prints them (tests/conftest.py), so they show in
+# the tail of a quiet run.
+REPORT: list = []
+
+
+def report(name: str, **counts) -> None:
+    """Record one test's exact / flagged counts for the end-of-run summary."""
+    REPORT.append((name, counts))
+
 
 def to_torch(x, device, kind=None):
     import torch

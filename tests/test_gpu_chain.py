@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from parity import TOL, check_chain, to_torch
+from parity import TOL, check_chain, report, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ def _run_chain(lib, case, want_c_star=True):
     return A.cpu().numpy(), y.cpu().numpy(), None if c is None else c.cpu().numpy()
 
 
-def _check_sampling(lib, case):
+def _check_sampling(lib, case, name=None):
     A, y, c = _run_chain(lib, case)
     t64, d64 = case.target.f64, case.draft.f64
     T = case.temperature
@@ -37,6 +37,9 @@ def _check_sampling(lib, case):
     ok = ~np.isnan(res.c_star)
     assert (np.isnan(c) == ~ok).all(), "c* NaN pattern differs"
     assert np.abs(c[ok] - res.c_star[ok]).max(initial=0.0) <= TOL
+    if name is not None:
+        report(name, requests=st.n, exact=st.exact, flagged_accept=st.flagged_accept,
+               flagged_sample=st.flagged_sample, max_abs_cstar_diff=float(np.abs(c[ok] - res.c_star[ok]).max(initial=0.0)))
     return st, A, y, res
 
 
@@ -158,7 +161,7 @@ def test_tv_accept_matches_oracle(lib):
 def test_long_vocab_single_request(lib):
     """R=1, gamma=7, V=151936 bf16, one planted +8 peak per position, T=1 and T=0."""
     case = synth.chain_long_vocab(seed=2)
-    _check_sampling(lib, case)
+    _check_sampling(lib, case, "chain R=1 gamma=7 V=151936 T=1")
     g = synth.chain_long_vocab(seed=2, temperature=0.0)
     _check_greedy(lib, g)
 
@@ -167,9 +170,7 @@ def test_batched_full_size(lib):
     """The benchmarked workload: R=64, gamma=7, V=151936 bf16, T=1, every request
     and every c*_{r,k} checked against the oracle."""
     case = synth.chain_batched(seed=3)
-    st, A, y, res = _check_sampling(lib, case)
-    print(f"\nbatched full size: {st.n} requests, {st.exact} exact, flagged accept {st.flagged_accept}, "
-          f"flagged sample {st.flagged_sample}, mean accepted {A.mean():.2f} (oracle {res.accepted.mean():.2f})")
+    st, A, y, res = _check_sampling(lib, case, "chain R=64 gamma=7 V=151936 T=1 (benchmarked workload)")
     assert st.exact >= st.n - 8
 
 
@@ -178,7 +179,7 @@ def test_full_vocab_ragged_lengths(lib):
     skipped positions, early bonus rows and l_r = 0 requests, T=1 and T=0."""
     case = synth.chain_batched(seed=111, R=16, gamma=7, ragged_lengths=True)
     assert (case.lengths == 0).any() or (case.lengths < 7).any()
-    st, A, y, res = _check_sampling(lib, case)
+    st, A, y, res = _check_sampling(lib, case, "chain R=16 ragged lengths V=151936 T=1")
     assert st.exact >= st.n - 2
     g = synth.chain_batched(seed=112, R=12, gamma=7, temperature=0.0, ragged_lengths=True)
     _check_greedy(lib, g)
@@ -187,5 +188,5 @@ def test_full_vocab_ragged_lengths(lib):
 def test_max_gamma_full_vocab(lib):
     """gamma = SPECV_MAX_GAMMA = 32 at V=151936 bf16: 33 positions per request."""
     case = synth.chain_batched(seed=113, R=3, gamma=32)
-    st, A, y, res = _check_sampling(lib, case)
+    st, A, y, res = _check_sampling(lib, case, "chain R=3 gamma=32 V=151936 T=1")
     assert st.exact >= st.n - 1

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from parity import TOL, to_torch
+from parity import TOL, check_chain, report, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -91,22 +91,24 @@ def _markov_check(lib, m, T, logits_dtype="f32"):
     ldt = torch.bfloat16 if logits_dtype == "bf16" else torch.float32
     toks, logits = lib.markov_draft(U, W1, W2, anchor, u, T, True, ldt)
     toks = toks.cpu().numpy()
-    L = logits.float().cpu().numpy().astype(np.float64)
-    U64, W164, W264 = m.U.f64, m.W1.f64, m.W2.f64
-    R, gamma, V = U64.shape
+    W164, W264 = m.W1.f64, m.W2.f64
+    R, gamma, V = m.U.shape
     prev = m.anchor.astype(np.int64)
     flagged = 0
     for k in range(gamma):
-        Lref, _, _, _ = oracle.markov_step(U64[:, k], W164, W264, prev, m.uniforms[:, k], max(T, 1.0))
+        # one step at a time keeps the host copies to one [R, V] slice
+        L_k = logits[:, k].float().cpu().numpy().astype(np.float64)
+        U_k = synth.bf16_bits_to_f64(m.U.raw[:, k])
+        Lref, _, _, _ = oracle.markov_step(U_k, W164, W264, prev, m.uniforms[:, k], max(T, 1.0))
         # float32 sum of `rank` exact bf16 products: |error| <= rank * 2^-24 * sum |products|
         # (recursive-summation bound), one rounding of U + bias, and the bf16 output rounding
         rank = W164.shape[1]
         acc_bound = rank * 2.0 ** -24 * (np.abs(W164[prev]) @ np.abs(W264))
         bound = 1e-6 * (1.0 + np.abs(Lref)) + acc_bound + (np.abs(Lref) * 2.0 ** -8 if logits_dtype == "bf16" else 0.0)
-        assert (np.abs(L[:, k] - Lref) <= bound).all(), f"step {k}: logits differ"
+        assert (np.abs(L_k - Lref) <= bound).all(), f"step {k}: logits differ"
         for r in range(R):
             y = int(toks[r, k])
-            Lr = L[r, k] if logits_dtype == "bf16" else Lref[r]
+            Lr = L_k[r] if logits_dtype == "bf16" else Lref[r]
             if T == 0.0:
                 g = int(np.argmax(Lref[r]))
                 if y != g:
@@ -168,29 +170,18 @@ def test_markov_long_vocab_single_request(lib):
         _markov_check(lib, m, T)
 
 
-def test_markov_large_batch_sampled_rows(lib):
-    """R=512, V=129280: the full DSpark drafting shape; every row's logits and tokens
-    are checked at each step (teacher-forced on the GPU's own tokens)."""
+def test_markov_large_batch_every_row(lib):
+    """R=512, gamma=7, V=129280, rank 256: the full DSpark drafting shape.  All
+    512 rows are checked at each of the 7 steps, teacher-forced on the GPU's own
+    previous tokens: logits within the float32 accumulation bound, every token
+    inside its CDF bracket, and draws that differ from the oracle's counted
+    (CDF steps here average 7.7e-6, so a uniform lands within 1e-5 of a boundary
+    often; a differing draw is allowed only there)."""
     m = synth.markov(seed=5, R=512, gamma=7, V=129280)
-    sel = np.arange(0, 512, 37)
-    import torch
-    dev = torch.device("cuda")
-    toks, logits = lib.markov_draft(to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev),
-                                    to_torch(m.anchor, dev, np.int32), to_torch(m.uniforms, dev, np.float32), 1.0)
-    toks = toks.cpu().numpy()
-    L = logits[torch.from_numpy(sel).to(dev)].cpu().numpy().astype(np.float64)
-    U64, W164, W264 = m.U.f64[sel], m.W1.f64, m.W2.f64
-    prev = m.anchor[sel].astype(np.int64)
-    for k in range(7):
-        Lref, _, _, _ = oracle.markov_step(U64[:, k], W164, W264, prev, m.uniforms[sel, k], 1.0)
-        assert (np.abs(L[:, k] - Lref) <= 1e-6 * (1 + np.abs(Lref))).all()
-        for i, r in enumerate(sel):
-            pr = oracle.softmax_t(Lref[i], 1.0)
-            C = np.cumsum(pr)
-            y = int(toks[r, k])
-            uu = float(m.uniforms[r, k])
-            assert (C[y - 1] if y > 0 else 0.0) - TOL <= uu < C[y] + TOL
-        prev = toks[sel, k].astype(np.int64)
+    _, flagged = _markov_check(lib, m, 1.0)
+    n = 512 * 7
+    report("markov R=512 gamma=7 V=129280 T=1 (every row)", draws=n, differing_from_oracle_within_tol=flagged)
+    assert flagged <= 3 + n // 20
 
 
 # --------------------------------------------------------------------------- scheduler
@@ -463,10 +454,12 @@ def test_confidence_head_bad_token(lib):
 def test_dspark_round_full_size(lib):
     """Markov drafting (R=512, gamma=7, V=129280, bf16 logits) -> scheduler -> chain
     verification with the scheduled lengths, all on the device.  The scheduler's
-    lengths are checked bit-exact against the oracle (its inputs are synthetic);
-    the verification of GPU-made drafts is checked through properties that hold
-    for any input: 0 <= A_r <= l_r, tokens in [0, V), c* in [0, 1] for k < l_r and
-    NaN beyond."""
+    lengths are checked bit-exact against the oracle (its inputs are synthetic).
+    The verification is checked against the oracle on the GPU's own drafts: the
+    bf16 draft logits and tokens it wrote, with the scheduled l_r, go through
+    oracle.verify_chain request by request (only the l_r + 1 live target rows and
+    l_r draft rows of each), and A_r, the emitted token and every c*_{r,k} must
+    agree under the flagged-threshold rule and the 1e-5 tolerance."""
     import torch
     dev = torch.device("cuda")
     R, G, V = 512, 7, 129280
@@ -480,14 +473,34 @@ def test_dspark_round_full_size(lib):
     lengths, _ = lib.schedule(to_torch(conf, dev, np.float32), to_torch(sps, dev, np.float64))
     ell = lengths.cpu().numpy()
     assert (ell == oracle.schedule(conf, sps).lengths).all()
-    u = to_torch(synth.uniform_f32(5, 44, (R, G + 1, 2)), dev, np.float32)
-    A, y, c = lib.verify_chain(target, dlog, toks, u, 1.0, lengths)
+    u_np = synth.uniform_f32(5, 44, (R, G + 1, 2))
+    A, y, c = lib.verify_chain(target, dlog, toks, to_torch(u_np, dev, np.float32), 1.0, lengths)
     A, y, c = A.cpu().numpy(), y.cpu().numpy(), c.cpu().numpy()
     t = toks.cpu().numpy()
+    d_bits = dlog.view(torch.int16).cpu().numpy().view(np.uint16)
+    del dlog
     assert ((t >= 0) & (t < V)).all()
-    assert ((A >= 0) & (A <= ell)).all() and ((y >= 0) & (y < V)).all()
     k = np.arange(G)[None, :]
     live = k < ell[:, None]
     assert np.isnan(c[~live]).all()
-    assert ((c[live] >= -1e-6) & (c[live] <= 1 + 1e-6)).all()
-    print(f"\ndspark round: sum l_r {ell.sum()}, mean accepted {A.mean():.2f}, mean c* {c[live].mean():.3f}")
+    tot = dict(requests=0, exact=0, flagged_accept=0, flagged_sample=0)
+    worst = 0.0
+    for r in range(R):
+        L = int(ell[r])
+        t64 = synth.bf16_bits_to_f64(tgt.raw[r:r + 1, :L + 1])
+        d64 = synth.bf16_bits_to_f64(d_bits[r:r + 1, :L])
+        x = t[r:r + 1, :L].astype(np.int64)
+        u = u_np[r:r + 1, :L + 1]
+        res = oracle.verify_chain(t64, d64, x, u, 1.0)
+        st = check_chain(A[r:r + 1], y[r:r + 1], res, lambda _r, kk: oracle.softmax_t(t64[0, kk], 1.0),
+                         lambda _r, kk: oracle.softmax_t(d64[0, kk], 1.0), u, np.array([L]))
+        for key in ("exact", "flagged_accept", "flagged_sample"):
+            tot[key] += getattr(st, key)
+        tot["requests"] += 1
+        if L:
+            diff = np.abs(c[r, :L] - res.c_star[0])
+            worst = max(worst, float(diff.max()))
+            assert (diff <= TOL).all(), f"request {r}: c* differs by {diff.max()}"
+    report("dspark round R=512 gamma=7 V=129280 T=1 (verify of the GPU's drafts)", sum_l=int(ell.sum()),
+           max_abs_cstar_diff=worst, **tot)
+    assert tot["exact"] >= R - 16
