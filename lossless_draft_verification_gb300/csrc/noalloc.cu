@@ -8,8 +8,6 @@
 //  - plain C hosts with no device allocator of their own.
 // Every launch and kernel is that of specv_verify_chain; only where the
 // scratch lives differs.
-#include <atomic>
-
 #include <cuda_runtime.h>
 
 #include "host_common.h"
@@ -21,22 +19,19 @@ namespace {
 // instantiated in every device context that loads this module).
 static __device__ __align__(256) unsigned char g_verify_scratch[SPECV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Device address of this device's copy of g_verify_scratch.  The first call on
-// a device resolves it with cudaGetSymbolAddress (which may load the module);
-// later calls read the cached pointer.
+// Device address of the current device's copy of g_verify_scratch in the
+// current context.  The first call on a device loads the library's device
+// module there (the set-up step); after that cudaGetSymbolAddress is a host
+// lookup.  It runs on every call rather than being cached: after
+// cudaDeviceReset, or in another context on the same device, the buffer has
+// another address, and a stale one would send the kernels to unmapped memory.
 specv_status scratch_for_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPECV_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SPECV_ERR_UNSUPPORTED;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return SPECV_ERR_CUDA;
-    if (!specv::aligned_to(p, 256)) return SPECV_ERR_CUDA;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();                 // leave no pending error behind
+    return SPECV_ERR_CUDA;
   }
+  if (!specv::aligned_to(p, 256)) return SPECV_ERR_CUDA;
   *out = p;
   return SPECV_OK;
 }
@@ -56,8 +51,12 @@ extern "C" specv_status specv_verify_chain_noalloc(const void* target_logits, co
   const size_t need = specv_verify_chain_workspace_size(R, gamma, V, dtype);
   if (need == 0) return SPECV_ERR_INVALID_ARG;
   if (need > SPECV_NOALLOC_SCRATCH_BYTES) return SPECV_ERR_SCRATCH_LIMIT;
+  // A device without an sm_103a image reports SPECV_ERR_UNSUPPORTED before
+  // the symbol lookup, which would fail there.
+  specv_status s = specv::check_device();
+  if (s != SPECV_OK) return s;
   void* scratch = nullptr;
-  const specv_status s = scratch_for_current_device(&scratch);
+  s = scratch_for_current_device(&scratch);
   if (s != SPECV_OK) return s;
   // The only word that must start at zero, the device error word in the first
   // 256 bytes, is cleared by the first kernel of every call.
