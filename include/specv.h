@@ -56,7 +56,9 @@
  *    arithmetic is float32; argmax compares the stored values exactly and
  *    resolves ties to the lowest token id.  Logits must be finite.
  *  - Thread-safe: no global state other than a per-device capability cache
- *    and the built-in scratch of specv_verify_chain_noalloc.
+ *    and the built-in scratch of specv_verify_chain_noalloc.  The one
+ *    exception: specv_verify_chain_noalloc calls on one device share that
+ *    scratch, so they must be serialised (see its section).
  */
 #ifndef SPECV_H_
 #define SPECV_H_
@@ -159,9 +161,12 @@ SPECV_API specv_status specv_verify_chain(const void* target_logits, const void*
  * memory-pool callback, servers that forbid device allocation once their
  * weights and KV cache are placed, C hosts without a device allocator.
  *
- * Set-up: the first call on each device (with that device current) looks up
- *   the buffer's device address with cudaGetSymbolAddress, which may load the
- *   library's device module; make that first call outside any stream capture.
+ * Set-up: the first call on each device (with that device current) loads
+ *   the library's device module there through cudaGetSymbolAddress; make that
+ *   first call outside any stream capture.  Every call looks the buffer's
+ *   address up again (a host-side lookup once the module is loaded), so the
+ *   address stays right after cudaDeviceReset and in any context the caller
+ *   makes current.
  * Concurrency: all calls on one device share the one buffer.  Calls whose
  *   execution may overlap (different streams, or host threads enqueueing
  *   without ordering) race on it and give undefined results; serialise them
@@ -434,6 +439,24 @@ SPECV_API specv_status specv_read_device_error(const void* workspace, void* stre
 
 SPECV_API const char* specv_status_string(specv_status status);
 SPECV_API int specv_abi_version(void);
+
+/*
+ * specv_selftest_bounded_wait -- exercises the library's bounded device-side
+ * wait (the pages have no counterpart: this is a failure-detection check).
+ *
+ * One thread initialises an mbarrier that expects one arrival and waits on
+ * its first phase with the same poll-limited wait the Markov kernel uses for
+ * its copies.  arrive == 0: nothing ever arrives, so after max_polls polls the
+ * wait gives up and the kernel records SPECV_ERR_TIMEOUT in the workspace
+ * error word and returns (no trap; the context stays usable).  arrive != 0:
+ * the thread arrives first, the wait succeeds and the word stays SPECV_OK.
+ *   max_polls in [1, 65536]; workspace >= 256 bytes, 256-byte aligned.
+ * Errors: SPECV_ERR_INVALID_ARG for a bad argument, SPECV_ERR_UNSUPPORTED off
+ * sm_103, SPECV_ERR_CUDA for a launch failure.  Read the outcome with
+ * specv_read_device_error.
+ */
+SPECV_API specv_status specv_selftest_bounded_wait(uint32_t max_polls, int arrive, void* workspace,
+                                                   size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ __all__ = [
     "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_schedule_global", "specv_prune_threshold",
     "specv_confidence_head_workspace_size", "specv_confidence_head", "specv_dart_tree_workspace_size",
     "specv_dart_tree",
-    "specv_read_device_error",
+    "specv_read_device_error", "specv_selftest_bounded_wait",
     "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
     "specv_shard_argmax_combine",
     "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "schedule_global",
@@ -69,6 +69,7 @@ EXPORTED = {
     "specv_confidence_head": (_c_int, [_vp, _vp, _vp, _c_float, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                        _vp, _c_size, _vp]),
     "specv_read_device_error": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
+    "specv_selftest_bounded_wait": (_c_int, [ctypes.c_uint32, _c_int, _vp, _c_size, _vp]),
     "specv_status_string": (ctypes.c_char_p, [_c_int]),
     "specv_abi_version": (_c_int, []),
     "specv_shard_combine_normalisers": (_c_int, [_vp, _c_int, _c_int, _vp]),
@@ -198,6 +199,10 @@ def specv_dart_tree(draft_logits, dtype, R, d, V, temperature, k, w, theta, pare
 
 def specv_read_device_error(workspace, stream, status_out):
     return _call("specv_read_device_error", workspace, stream, status_out)
+
+
+def specv_selftest_bounded_wait(max_polls, arrive, workspace, workspace_bytes, stream):
+    return _call("specv_selftest_bounded_wait", max_polls, arrive, workspace, workspace_bytes, stream)
 
 
 def specv_status_string(status):

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include "common.cuh"
 #include "host_common.h"
 #include "specv.h"
 
@@ -56,4 +57,30 @@ extern "C" specv_status specv_read_device_error(const void* workspace, void* str
   if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SPECV_ERR_CUDA;
   *status_out = v;
   return SPECV_OK;
+}
+
+namespace {
+
+// One thread waits on a barrier that nothing arrives at (unless `arrive`),
+// with the poll-limited wait of the production kernels.
+__global__ void bounded_wait_kernel(uint32_t max_polls, int arrive, void* workspace) {
+  __shared__ uint64_t bar;
+  specv::mbar_init(&bar, 1);
+  specv::fence_mbar_init();
+  if (arrive) specv::mbar_arrive(&bar);
+  const bool ok = specv::mbar_wait_parity(&bar, 0, max_polls);
+  *reinterpret_cast<int*>(workspace) = ok ? SPECV_OK : SPECV_ERR_TIMEOUT;
+}
+
+}  // namespace
+
+extern "C" specv_status specv_selftest_bounded_wait(uint32_t max_polls, int arrive, void* workspace,
+                                                   size_t workspace_bytes, void* stream) {
+  if (max_polls < 1 || max_polls > 65536 || !workspace || workspace_bytes < 256 ||
+      !specv::aligned_to(workspace, 256))
+    return SPECV_ERR_INVALID_ARG;
+  const specv_status s = specv::check_device();
+  if (s != SPECV_OK) return s;
+  bounded_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(max_polls, arrive, workspace);
+  return cudaGetLastError() == cudaSuccess ? SPECV_OK : SPECV_ERR_CUDA;
 }
