@@ -278,17 +278,77 @@ def _raise(status, where):
         raise SpecvError(status, where)
 
 
+def _verify_chain_host_chunked(target, draft, draft_tokens, uniforms, temperature, lengths, want_c_star, chunks,
+                               stream):
+    """Host inputs, requests split into `chunks` groups: group i's host-to-device
+    copies run on copy stream i % 2 while the verification of group i - 1 runs
+    on the compute stream, so the copies overlap the kernels (and the two copy
+    streams can use two copy engines)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    comp = stream if stream is not None else torch.cuda.current_stream(dev)
+    R, P, V = target.shape
+    gamma = P - 1
+    nb = target.is_pinned()
+    d_t = torch.empty(target.shape, dtype=target.dtype, device=dev)
+    d_d = None if draft is None else torch.empty(draft.shape, dtype=draft.dtype, device=dev)
+    d_x = torch.empty(draft_tokens.shape, dtype=draft_tokens.dtype, device=dev)
+    d_u = None if uniforms is None else torch.empty(uniforms.shape, dtype=uniforms.dtype, device=dev)
+    d_l = None if lengths is None else torch.empty(lengths.shape, dtype=lengths.dtype, device=dev)
+    acc = torch.empty(R, dtype=torch.int32, device=dev)
+    tok = torch.empty(R, dtype=torch.int32, device=dev)
+    cst = torch.empty(R, gamma, dtype=torch.float32, device=dev) if want_c_star else None
+    code = _dtype_code(target)
+    copies = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    for c in copies:
+        c.wait_stream(comp)                 # the device buffers were allocated on the compute stream
+    step = -(-R // chunks)
+    ws = None
+    for i, r0 in enumerate(range(0, R, step)):
+        r1 = min(R, r0 + step)
+        cs = copies[i % 2]
+        with torch.cuda.stream(cs):
+            for d, h in ((d_t, target), (d_d, draft), (d_x, draft_tokens), (d_u, uniforms), (d_l, lengths)):
+                if d is not None:
+                    d[r0:r1].copy_(h[r0:r1], non_blocking=nb)
+        ev = torch.cuda.Event()
+        ev.record(cs)
+        comp.wait_event(ev)
+        n = r1 - r0
+        nbytes = specv_verify_chain_workspace_size(n, gamma, V, code)
+        if nbytes == 0:
+            raise SpecvError(SPECV_ERR_UNSUPPORTED, "specv_verify_chain_workspace_size")
+        if ws is None:
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        sl = lambda t: None if t is None else t[r0:r1]
+        st = specv_verify_chain(_p(sl(d_t)), _p(sl(d_d)), code, _p(sl(d_x)), _p(sl(d_l)), _p(sl(d_u)), n, gamma, V,
+                                float(temperature), _p(sl(acc)), _p(sl(tok)), _p(sl(cst)), _p(ws), ws.numel(),
+                                comp.cuda_stream)
+        _raise(st, "specv_verify_chain")
+    for t in (d_t, d_d, d_x, d_u, d_l):
+        if t is not None:
+            for c in copies:
+                t.record_stream(c)
+    with torch.cuda.stream(comp):
+        return acc.cpu(), tok.cpu(), None if cst is None else cst.cpu()
+
+
 def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, lengths=None, want_c_star: bool = True,
-                 workspace=None, stream=None, out=None):
+                 workspace=None, stream=None, out=None, chunks: int = 1):
     """Chain speculative sampling (see specv_verify_chain in include/specv.h).
 
     target [R, gamma+1, V], draft [R, gamma, V] (bf16 or float32), draft_tokens
     [R, gamma] int32, uniforms [R, gamma+1, 2] float32 (None at T = 0), lengths
     [R] int32 or None.  Returns (accepted_len [R], out_token [R], c_star [R, gamma]
     or None) on the inputs' device.  Host (CPU) inputs are copied to the current
-    CUDA device first and the results copied back."""
+    CUDA device first and the results copied back; with chunks > 1 the requests
+    go in that many groups whose copies overlap the previous group's kernels
+    (pinned host tensors make the copies asynchronous)."""
     torch = _torch()
     host = target.device.type == "cpu"
+    if host and chunks > 1 and out is None and workspace is None and target.shape[0] > 1:
+        return _verify_chain_host_chunked(target, draft, draft_tokens, uniforms, temperature, lengths, want_c_star,
+                                          min(int(chunks), target.shape[0]), stream)
     if host:
         dev = torch.device("cuda", torch.cuda.current_device())
         nb = target.is_pinned()

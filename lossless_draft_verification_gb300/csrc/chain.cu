@@ -617,8 +617,17 @@ __global__ void __launch_bounds__(NW * 32, 2) chain_stats_pipe_kernel(PipeArgs p
     }
     ++processed;
   }
-  // Every store into this CTA's partials precedes the barrier of the last
-  // item, and all reads are local: no exit barrier is needed.
+  // No exit barrier is needed, because of one invariant: every CTA of a
+  // cluster walks the same item sequence.  The walk depends only on the
+  // cluster index, the grid's cluster count and the call's lengths (the
+  // compacted walk's prefix is computed identically in every CTA from the same
+  // lengths), and the kind of each item (skip, row pair, bonus row) is decided
+  // from the same values, so every CTA executes the same number of cluster
+  // barriers.  A CTA's last remote store into a peer's partials precedes its
+  // arrive at the last barrier, and the peer reads them only after its wait,
+  // so no CTA can exit while a peer may still store into its shared memory.
+  // (Removing the per-item barrier breaks this: a remote store then can reach
+  // a CTA that has already exited.)
   cp_async_wait_all();
   pdl_launch_dependents();
 }
