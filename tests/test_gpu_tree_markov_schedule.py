@@ -181,7 +181,7 @@ def test_markov_large_batch_every_row(lib):
     _, flagged = _markov_check(lib, m, 1.0)
     n = 512 * 7
     report("markov R=512 gamma=7 V=129280 T=1 (every row)", draws=n, differing_from_oracle_within_tol=flagged)
-    assert flagged <= 3 + n // 20
+    assert flagged <= 3 + n // 100                  # measured on GB300: 17 of 3584
 
 
 # --------------------------------------------------------------------------- scheduler
