@@ -636,23 +636,29 @@ def run_workload(args):
         ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                 "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
-    elif w == "markov":
+    elif w in ("markov", "markov_tokens"):
         Rm, Gm, Vm, rank = 512, args.positions or 7, 129280, 256
         m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
         U, W1, W2 = bf(m.U), bf(m.W1), bf(m.W2)
         anchor, u = td(m.anchor, np.int32), td(m.uniforms, np.float32)
         toks = torch.empty(Rm, Gm, dtype=torch.int32, device=dev)
-        logits = torch.empty(Rm, Gm, Vm, dtype=torch.float32, device=dev)
+        keep = w == "markov"
+        logits = torch.empty(Rm, Gm, Vm, dtype=torch.float32, device=dev) if keep else None
         nb = specv.specv_markov_draft_workspace_size(Rm, Gm, Vm, rank)
         ws = torch.empty(nb, dtype=torch.uint8, device=dev)
         call = lambda: check(specv.specv_markov_draft(U.data_ptr(), W1.data_ptr(), W2.data_ptr(), anchor.data_ptr(),
                                                       u.data_ptr(), Rm, Gm, Vm, rank, 1.0, toks.data_ptr(),
-                                                      logits.data_ptr(), specv.SPECV_F32, ws.data_ptr(), nb, sp),
+                                                      logits.data_ptr() if keep else None, specv.SPECV_F32,
+                                                      ws.data_ptr(), nb, sp),
                              "specv_markov_draft")
-        algo = Gm * (Rm * Vm * 2 + rank * Vm * 2 + Rm * Vm * 4)
+        if keep:
+            algo = Gm * (Rm * Vm * 2 + rank * Vm * 2 + Rm * Vm * 4)
+        else:
+            algo = Gm * Rm * Vm * 2 + rank * Vm * 2     # U once per step, W2 once (it stays in L2 across steps)
         flops = Gm * 2 * Rm * rank * Vm
         units, unit, metric = Rm * Gm, "tokens/s", "Markov-head drafting: draft tokens/sec"
-        desc = f"DSpark Markov head: R=512, gamma={Gm}, V=129280, rank 256, T=1, float32 logits out"
+        desc = (f"DSpark Markov head: R=512, gamma={Gm}, V=129280, rank 256, T=1, "
+                + ("float32 logits out" if keep else "tokens only (no logits kept)"))
         launches, kernel = 2 * Gm, "markov logits + sample (whole call)"
         ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -800,7 +806,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "greedy", "tv", "tree", "markov", "schedule", "schedule_global", "prune", "confidence", "dart", "dspark"])
+                    choices=["chain", "greedy", "tv", "tree", "markov", "markov_tokens", "schedule", "schedule_global", "prune", "confidence", "dart", "dspark"])
     ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     world = os.environ.get("WORLD_SIZE")

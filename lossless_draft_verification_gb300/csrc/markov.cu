@@ -55,7 +55,8 @@ struct MarkovArgs {
   const int32_t* anchor;      // [R]
   const float* uniforms;      // [R, gamma]
   int32_t* tokens;            // [R, gamma]
-  void* logits;               // output logits base: [R, lstride_r] rows of V (f32 or bf16)
+  void* logits;               // output logits base: [R, lstride_r] rows of V (f32 or bf16); null: none kept
+                              // (tensor-core form only: the sampler recomputes its tile)
   int logits_bf16;
   long lstride_r;             // elements between consecutive requests in `logits`
   long step_off;              // element offset of this step's row inside a request
@@ -188,8 +189,11 @@ __global__ void __launch_bounds__(kMkThreads) markov_logits_kernel(MarkovArgs a)
 constexpr int kSampleThreads = 256;
 constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kSampleMaxPer = 16;     // tiles per thread: at most 4096 tiles per row
+constexpr int kSampleMaxRank = 256;   // rank of the tensor-core form, whose tiles may be recomputed
 
 __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArgs a) {
+  __shared__ float s_e[kSampleMaxRank];  // W1[x_{k-1}] when the tile is recomputed
+  __shared__ float s_chunk[4][64];       // per-rank-chunk sums, then the recomputed tile
   __shared__ float s_f[kSampleWarps];
   __shared__ int s_i[kSampleWarps];
   __shared__ int s_sel;
@@ -312,8 +316,40 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
   }
   __syncthreads();
   const int sel = s_sel;
-  if (warp != 0) return;                   // warp 0 triggers the next step once the token is written
   bool bad = bad_in || sel < 0;
+  if (a.logits == nullptr) {
+    // No logits were kept (tensor-core form, tile_w = 64): recompute the
+    // selected tile's 64 logits, L(v) = U_k(v) + sum_j W1[x_{k-1}, j] W2[j, v],
+    // float32 products summed in four rank chunks (one per group of 64
+    // threads), then the chunks in order.
+    if (!bad)
+      for (int j = threadIdx.x; j < a.rank; j += kSampleThreads)
+        s_e[j] = bf16_to_f32(a.W1[size_t(x_prev) * a.rank + j]);
+    __syncthreads();
+    const int c = threadIdx.x & 63, q = threadIdx.x >> 6;
+    const int v = sel * 64 + c;
+    if (!bad && v < a.V) {
+      const int j0 = q * (a.rank >> 2), j1 = j0 + (a.rank >> 2);
+      const uint16_t* w2 = a.W2 + v;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+      for (int j = j0; j < j1; j += 2) {
+        acc0 = fmaf(s_e[j], bf16_to_f32(w2[size_t(j) * a.V]), acc0);
+        acc1 = fmaf(s_e[j + 1], bf16_to_f32(w2[size_t(j + 1) * a.V]), acc1);
+      }
+      s_chunk[q][c] = acc0 + acc1;
+    }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+      float x = neg_inf();
+      if (!bad && v < a.V)
+        x = bf16_to_f32(a.U[(size_t(r) * a.gamma + (a.k - 1)) * a.V + v]) +
+            ((s_chunk[0][c] + s_chunk[1][c]) + (s_chunk[2][c] + s_chunk[3][c]));
+      s_chunk[0][c] = x;                       // the tile's logits, in column order
+    }
+    __syncthreads();
+  }
+  if (warp != 0) return;                   // warp 0 triggers the next step once the token is written
   if (!bad) {
     // rescan the selected tile's columns in index order
     const MarkovPart p = part[sel];
@@ -327,8 +363,9 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
       const int v = sel * a.tile_w + lane * cpl + c;
       float x = neg_inf();
       if (c < cpl && v < a.V) {
-        x = a.logits_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.logits)[rowbase + v])
-                          : reinterpret_cast<const float*>(a.logits)[rowbase + v];
+        if (a.logits == nullptr) x = s_chunk[0][lane * cpl + c];
+        else x = a.logits_bf16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.logits)[rowbase + v])
+                               : reinterpret_cast<const float*>(a.logits)[rowbase + v];
       }
       w[c] = __fmul_rn(ex2(fmaf(x, a.c2, -p.a)), sc);
       ls += w[c];
@@ -369,10 +406,14 @@ constexpr int kTcThreads = (kTcEpiWarps + 2) * 32;   // + TMA warp + MMA warp
 constexpr uint32_t kTcTmemCols = 128;     // two accumulator buffers of 64 columns
 constexpr uint32_t kTcRowBytes = 128;     // one swizzled row
 constexpr size_t kTcSmemE = size_t(kTcMaxKC) * kTcBM * kTcRowBytes;        // 64 KB: W1 rows
-constexpr size_t kTcSmemB = size_t(2) * kTcMaxKC * 64 * kTcRowBytes;       // 64 KB: W2 tiles [rank][64], two stages
-constexpr size_t kTcSmemU = size_t(2) * kTcBM * kTcRowBytes;               // 32 KB: U tiles, two stages
+constexpr size_t kTcStageB = size_t(kTcMaxKC) * 64 * kTcRowBytes;          // 32 KB: one W2 tile [rank][64]
+constexpr size_t kTcStageU = size_t(kTcBM) * kTcRowBytes;                   // 16 KB: one U tile
 constexpr size_t kTcSmemL = size_t(kTcEpiWarps) * 2 * 32 * kTcRowBytes;    // 64 KB: logit staging per warp
-constexpr size_t kTcSmem = kTcSmemE + kTcSmemB + kTcSmemU + kTcSmemL + 1024;
+// NS stages of the W2 and U rings: two when logits are stored (the staging
+// takes the rest of shared memory), three when they are not
+__host__ __device__ constexpr size_t tc_smem(int ns, bool store) {
+  return kTcSmemE + size_t(ns) * (kTcStageB + kTcStageU) + (store ? kTcSmemL : 0) + 1024;
+}
 constexpr uint32_t kTcMaxPolls = 1u << 22;   // bound on every mbarrier wait
 constexpr uint32_t kTcIdesc = tc::idesc_bf16_f32(kTcBM, kTcBN, true);   // B = W2, MN-major
 
@@ -387,20 +428,21 @@ struct MarkovTcArgs {
 // 16-byte granule g of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int g) { return uint32_t(r) * kTcRowBytes + (uint32_t(g ^ (r & 7)) << 4); }
 
+template <int NS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
                      const __grid_constant__ CUtensorMap tmap_l, MarkovTcArgs ta) {
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
-  __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_tfull[2], bar_tempty[2], bar_ufull[2], bar_uempty[2],
-      bar_done;
+  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_tfull[2], bar_tempty[2], bar_ufull[NS],
+      bar_uempty[NS], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_err;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
   uint8_t* sB = sE + kTcSmemE;                      // [stage][rank][128 B]: W2[k, n0 .. n0+64)
-  uint8_t* sU = sB + kTcSmemB;                      // [stage][128 rows][128 B]  (64 bf16 per row)
-  uint8_t* sL = sU + kTcSmemU;                      // [warp][2 halves][32 rows][128 B]  (32 floats per row)
+  uint8_t* sU = sB + NS * kTcStageB;                // [stage][128 rows][128 B]  (64 bf16 per row)
+  uint8_t* sL = sU + NS * kTcStageU;                // [warp][2 halves][32 rows][128 B]  (32 floats per row)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb = blockIdx.x / ta.per_mb, j0 = blockIdx.x - (blockIdx.x / ta.per_mb) * ta.per_mb;
@@ -408,13 +450,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], 1);
-      mbar_init(&bar_tfull[i], 1);
-      mbar_init(&bar_tempty[i], 4);
       mbar_init(&bar_ufull[i], 1);
       mbar_init(&bar_uempty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 4);
     }
     mbar_init(&bar_done, 1);
     s_err = 0;
@@ -449,46 +493,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kTcEpiWarps) {
     // ---- TMA producer: W2[:, t*64 .. +64) (MMA operand) and U_k[rows, t*64 .. +64) (epilogue)
     if (lane == 0) {
+      // W2 is read by every step: keep it in L2 ahead of U, which is read once
+      const uint64_t keep = tc::policy_evict_last(), stream_once = tc::policy_evict_first();
       int i = 0;
       for (int t = j0; t < ta.ntiles; t += ta.per_mb, ++i) {
-        const int s = i & 1;
-        const uint32_t fresh = ((i >> 1) & 1) ^ 1;
+        const int s = i % NS;
+        const uint32_t fresh = ((i / NS) & 1) ^ 1;
         if (!mbar_wait_parity(&bar_empty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
         mbar_arrive_expect_tx(&bar_full[s], uint32_t(ta.nkc) * 64 * kTcRowBytes);
         for (int kc = 0; kc < ta.nkc; ++kc)     // 64 k-rows of 64 columns per box
-          tc::tma_load_2d(sB + (size_t(s) * kTcMaxKC + kc) * (64 * kTcRowBytes), &tmap_w2, t * kTcBN, kc * 64,
-                          &bar_full[s]);
+          tc::tma_load_2d_hint(sB + size_t(s) * kTcStageB + size_t(kc) * (64 * kTcRowBytes), &tmap_w2, t * kTcBN,
+                               kc * 64, &bar_full[s], keep);
         if (!mbar_wait_parity(&bar_uempty[s], fresh, kTcMaxPolls)) { s_err = 1; break; }
         mbar_arrive_expect_tx(&bar_ufull[s], kTcBM * kTcRowBytes);
-        tc::tma_load_3d(sU + size_t(s) * (kTcBM * kTcRowBytes), &tmap_u, t * kTcBN, a.k - 1, row0, &bar_ufull[s]);
+        tc::tma_load_3d_hint(sU + size_t(s) * kTcStageU, &tmap_u, t * kTcBN, a.k - 1, row0, &bar_ufull[s],
+                             stream_once);
       }
       // every issued copy has landed before the CTA may leave
-      for (int d = (i >= 2 ? i - 2 : 0); d < i; ++d) {
-        if (!mbar_wait_parity(&bar_full[d & 1], (d >> 1) & 1, kTcMaxPolls)) s_err = 1;
-        if (!mbar_wait_parity(&bar_ufull[d & 1], (d >> 1) & 1, kTcMaxPolls)) s_err = 1;
+      for (int d = (i >= NS ? i - NS : 0); d < i; ++d) {
+        if (!mbar_wait_parity(&bar_full[d % NS], (d / NS) & 1, kTcMaxPolls)) s_err = 1;
+        if (!mbar_wait_parity(&bar_ufull[d % NS], (d / NS) & 1, kTcMaxPolls)) s_err = 1;
       }
     }
   } else if (warp == kTcEpiWarps + 1) {
     // ---- MMA issuer
     if (lane == 0) {
+      // Descriptors are linear in their 14-bit start-address field (address / 16),
+      // so each MMA's descriptor is a base plus a constant: A chunk kc at
+      // +kc * 16 KB, 32-byte K step inside a 128-byte row; B k-group kk at
+      // +kk * 2 KB.  Computing them once keeps the issue loop short.
+      const uint64_t da0 = tc::smem_desc_k_sw128(smem_addr(sE));
+      uint64_t db0[NS];
+#pragma unroll
+      for (int st = 0; st < NS; ++st) db0[st] = tc::smem_desc_mn_sw128(smem_addr(sB) + uint32_t(st) * kTcStageB, 1024, 64 * 64 * 2);
       int i = 0;
       for (int t = j0; t < ta.ntiles; t += ta.per_mb, ++i) {
-        const int s = i & 1;
-        if (!mbar_wait_parity(&bar_tempty[s], ((i >> 1) & 1) ^ 1, kTcMaxPolls) ||
-            !mbar_wait_parity(&bar_full[s], (i >> 1) & 1, kTcMaxPolls)) {
+        const int s = i % NS, tb = i & 1;         // W2 stage, TMEM accumulator buffer
+        if (!mbar_wait_parity(&bar_tempty[tb], ((i >> 1) & 1) ^ 1, kTcMaxPolls) ||
+            !mbar_wait_parity(&bar_full[s], (i / NS) & 1, kTcMaxPolls)) {
           s_err = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t aE = smem_addr(sE), aB = smem_addr(sB) + uint32_t(s) * kTcMaxKC * 64 * kTcRowBytes;
+        uint64_t dbs = db0[0];
+#pragma unroll
+        for (int st = 1; st < NS; ++st)
+          if (s == st) dbs = db0[st];
+        const uint32_t dtm = tmem + uint32_t(tb * kTcBN);
         for (int kk = 0; kk < ta.nkc * 4; ++kk) {
-          const uint64_t da = tc::smem_desc_k_sw128(aE + uint32_t(kk >> 2) * (kTcBM * kTcRowBytes) + uint32_t(kk & 3) * 32);
-          // 16 k-rows per instruction: two 1024-byte groups further along K
-          const uint64_t db = tc::smem_desc_mn_sw128(aB + uint32_t(kk) * 2048, 1024, 64 * 64 * 2);
-          tc::mma_bf16(tmem + uint32_t(s * kTcBN), da, db, kTcIdesc, kk > 0 ? 1u : 0u);
+          // A: chunk kk / 4 (16 KB apart), 32-byte K step; B: 16 k-rows = two 1024-byte groups further along K
+          const uint64_t da = da0 + uint64_t((kk >> 2) * (kTcBM * kTcRowBytes / 16) + (kk & 3) * 2);
+          const uint64_t db = dbs + uint64_t(kk * (2048 / 16));
+          tc::mma_bf16(dtm, da, db, kTcIdesc, kk > 0 ? 1u : 0u);
         }
         tc::commit(&bar_empty[s]);            // the W2 stage is free once these MMAs have read it
-        tc::commit(&bar_tfull[s]);            // the accumulator is ready for the epilogue
+        tc::commit(&bar_tfull[tb]);           // the accumulator is ready for the epilogue
       }
       tc::commit(&bar_done);
       if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
@@ -503,10 +562,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int i = g;
     for (int t = j0 + g * ta.per_mb; t < ta.ntiles; t += 2 * ta.per_mb, i += 2) {
       const int n0 = t * kTcBN;
-      const uint32_t ph = (i >> 1) & 1;
+      const int us = i % NS;                        // U stage of tile i (its accumulator buffer is g)
       // warp-uniform outcome: tcgen05.ld below needs all 32 lanes
-      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], ph, kTcMaxPolls) &&
-                                       mbar_wait_parity(&bar_ufull[g], ph, kTcMaxPolls))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], (i >> 1) & 1, kTcMaxPolls) &&
+                                       mbar_wait_parity(&bar_ufull[us], (i / NS) & 1, kTcMaxPolls))) {
         s_err = 1;
         break;
       }
@@ -517,58 +576,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::tmem_ld32(taddr + 32, acc1);
       tc::tmem_ld_wait();
       uint4 u[8];
-      const uint8_t* urow = sU + size_t(g) * (kTcBM * kTcRowBytes);
+      const uint8_t* urow = sU + size_t(us) * kTcStageU;
 #pragma unroll
       for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4*>(urow + sw128(rl, c));
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bar_tempty[g]);
-        mbar_arrive(&bar_uempty[g]);
+        mbar_arrive(&bar_uempty[us]);
       }
+      // L = U + acc, two columns per packed add
       float L[64];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t wv[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8; e += 2) {
           const int j = 8 * c + e;
-          const float ub = __uint_as_float(e & 1 ? (wv[e >> 1] & 0xFFFF0000u) : (wv[e >> 1] << 16));
-          float x = ub + (j < 32 ? acc0[j] : acc1[j - 32]);
-          if (a.logits_bf16) x = round_to_bf16(x);
-          L[j] = n0 + j < a.V ? x : neg_inf();
+          const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
+          const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
+          float2 x = add2(ub, ac);
+          if (a.logits_bf16) {
+            x.x = round_to_bf16(x.x);
+            x.y = round_to_bf16(x.y);
+          }
+          L[j] = x.x;
+          L[j + 1] = x.y;
         }
+      }
+      if (n0 + 64 > a.V) {                          // the last tile: columns past V read -inf
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (n0 + j >= a.V) L[j] = neg_inf();
       }
       // logits: this warp's 32 rows x 64 columns through swizzled staging, then TMA stores
-      if (lane == 0) tc::bulk_wait_read_all();     // the previous tile's stores have read the staging
-      __syncwarp();
-      if (a.logits_bf16) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 o;
-          o.x = (__float_as_uint(L[8 * c + 0]) >> 16) | (__float_as_uint(L[8 * c + 1]) & 0xFFFF0000u);
-          o.y = (__float_as_uint(L[8 * c + 2]) >> 16) | (__float_as_uint(L[8 * c + 3]) & 0xFFFF0000u);
-          o.z = (__float_as_uint(L[8 * c + 4]) >> 16) | (__float_as_uint(L[8 * c + 5]) & 0xFFFF0000u);
-          o.w = (__float_as_uint(L[8 * c + 6]) >> 16) | (__float_as_uint(L[8 * c + 7]) & 0xFFFF0000u);
-          *reinterpret_cast<uint4*>(stage + sw128(lane, c)) = o;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<float4*>(stage + (c >> 3) * (32 * kTcRowBytes) + sw128(lane, c & 7)) =
-              make_float4(L[4 * c], L[4 * c + 1], L[4 * c + 2], L[4 * c + 3]);
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int z = row0 + qd * 32;
+      if (NS == 2 && a.logits != nullptr) {          // the staging exists only in the two-stage layout
+        if (lane == 0) tc::bulk_wait_read_all();     // the previous tile's stores have read the staging
+        __syncwarp();
         if (a.logits_bf16) {
-          tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 o;
+            o.x = (__float_as_uint(L[8 * c + 0]) >> 16) | (__float_as_uint(L[8 * c + 1]) & 0xFFFF0000u);
+            o.y = (__float_as_uint(L[8 * c + 2]) >> 16) | (__float_as_uint(L[8 * c + 3]) & 0xFFFF0000u);
+            o.z = (__float_as_uint(L[8 * c + 4]) >> 16) | (__float_as_uint(L[8 * c + 5]) & 0xFFFF0000u);
+            o.w = (__float_as_uint(L[8 * c + 6]) >> 16) | (__float_as_uint(L[8 * c + 7]) & 0xFFFF0000u);
+            *reinterpret_cast<uint4*>(stage + sw128(lane, c)) = o;
+          }
         } else {
-          tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
-          tc::tma_store_3d(&tmap_l, n0 + 32, ta.lz, z, stage + 32 * kTcRowBytes);
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<float4*>(stage + (c >> 3) * (32 * kTcRowBytes) + sw128(lane, c & 7)) =
+                make_float4(L[4 * c], L[4 * c + 1], L[4 * c + 2], L[4 * c + 3]);
         }
-        tc::bulk_commit();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int z = row0 + qd * 32;
+          if (a.logits_bf16) {
+            tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
+          } else {
+            tc::tma_store_3d(&tmap_l, n0, ta.lz, z, stage);
+            tc::tma_store_3d(&tmap_l, n0 + 32, ta.lz, z, stage + 32 * kTcRowBytes);
+          }
+          tc::bulk_commit();
+        }
       }
       if (!rv) continue;
       MarkovPart mpart;
@@ -581,22 +653,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mpart.a = m;
         mpart.b = __int_as_float(idx);
       } else {
-        float m = L[0];
+        // tree maximum (short dependency chains), then four packed partial sums
+        float mx[16];
 #pragma unroll
-        for (int j = 1; j < 64; ++j) m = fmaxf(m, L[j]);
-        const float m_c2 = m * a.c2;
-        float z0 = 0.f, z1 = 0.f;
+        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(L[j], L[j + 16]), fmaxf(L[j + 32], L[j + 48]));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+        const float m_c2 = mx[0] * a.c2;
+        const float2 c2v = make_float2(a.c2, a.c2), mv = make_float2(-m_c2, -m_c2);
+        float2 z[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
-          z0 += ex2(fmaf(L[j], a.c2, -m_c2));
-          z1 += ex2(fmaf(L[j + 1], a.c2, -m_c2));
+          const float2 tt = fma2(make_float2(L[j], L[j + 1]), c2v, mv);
+          z[(j >> 1) & 3] = add2(z[(j >> 1) & 3], make_float2(ex2(tt.x), ex2(tt.y)));
         }
         mpart.a = m_c2;
-        mpart.b = z0 + z1;
+        mpart.b = ((z[0].x + z[0].y) + (z[1].x + z[1].y)) + ((z[2].x + z[2].y) + (z[3].x + z[3].y));
       }
       a.part[size_t(r) * a.ntile + t] = mpart;
     }
-    if (lane == 0) tc::bulk_wait_all();           // logits written before the sampler reads them
+    if (NS == 2 && lane == 0 && a.logits != nullptr) tc::bulk_wait_all();   // logits written before the sampler reads them
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -697,7 +775,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     a.logits_bf16 = logits_out_dtype == SPECV_BF16;
     a.lstride_r = long(gamma) * V;
   } else {
-    a.logits = base + L.scratch_off;            // [R, V] float32, reused by every step
+    a.logits = base + L.scratch_off;            // [R, V] float32, reused by every step (CUDA-core form)
     a.logits_bf16 = 0;
     a.lstride_r = V;
   }
@@ -750,10 +828,16 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SPECV_ERR_CUDA;
     }
-    if (cudaFuncSetAttribute(reinterpret_cast<void*>(&markov_tc_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kTcSmem)) != cudaSuccess)
+    // three-stage rings when no logits are staged for storing, else two
+    const bool store = draft_logits != nullptr;
+    void* tc_fn = store ? reinterpret_cast<void*>(&markov_tc_kernel<2>) : reinterpret_cast<void*>(&markov_tc_kernel<3>);
+    const size_t tc_bytes = store ? tc_smem(2, true) : tc_smem(3, false);
+    if (cudaFuncSetAttribute(tc_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tc_bytes)) != cudaSuccess)
       return SPECV_ERR_CUDA;
     MarkovTcArgs ta;
+    // With no logits kept the epilogue writes only the tile partials and the
+    // sampler recomputes the 64 logits of the tile it draws from.
+    if (!draft_logits) a.logits = nullptr;
     a.tile_w = kTcBN;
     a.ntile = (V + kTcBN - 1) / kTcBN;
     ta.nkc = rank / 64;
@@ -778,8 +862,8 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       void* targs[] = {&tmap_w2, &tmap_u, &tmap_l, &ta};
       cfg.gridDim = g1;
       cfg.blockDim = dim3(kTcThreads);
-      cfg.dynamicSmemBytes = kTcSmem;
-      if (cudaLaunchKernelExC(&cfg, reinterpret_cast<void*>(&markov_tc_kernel), targs) != cudaSuccess)
+      cfg.dynamicSmemBytes = tc_bytes;
+      if (cudaLaunchKernelExC(&cfg, tc_fn, targs) != cudaSuccess)
         return SPECV_ERR_CUDA;
       void* sargs[] = {&a};
       cfg.gridDim = dim3(unsigned(R));

@@ -184,6 +184,63 @@ def test_markov_large_batch_every_row(lib):
     assert flagged <= 3 + n // 100                  # measured on GB300: 17 of 3584
 
 
+def _markov_tokens_only_check(lib, m, T):
+    """Drafting with no logits kept: the tensor-core epilogue writes only tile
+    partials and the sampler recomputes the 64 logits of the tile it draws
+    from.  Every token must lie in the oracle's CDF bracket (within 1e-5) for
+    the oracle's logits conditioned on the GPU's own previous token; tokens
+    that differ from the logits-kept call are counted."""
+    import torch
+    dev = torch.device("cuda")
+    args = (to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev), to_torch(m.anchor, dev, np.int32),
+            to_torch(m.uniforms, dev, np.float32), T)
+    toks, none = lib.markov_draft(*args, False)
+    assert none is None
+    toks = toks.cpu().numpy()
+    kept, _ = lib.markov_draft(*args, True)
+    kept = kept.cpu().numpy()
+    W164, W264 = m.W1.f64, m.W2.f64
+    R, gamma, V = m.U.shape
+    prev = m.anchor.astype(np.int64)
+    differ = 0
+    for k in range(gamma):
+        U_k = synth.bf16_bits_to_f64(m.U.raw[:, k])
+        Lref, _, _, _ = oracle.markov_step(U_k, W164, W264, prev, m.uniforms[:, k], max(T, 1.0))
+        for r in range(R):
+            y = int(toks[r, k])
+            if T == 0.0:
+                srt = np.sort(Lref[r])
+                assert Lref[r, y] >= srt[-1] - 2e-6 * (1 + abs(srt[-1])), "argmax differs beyond a near tie"
+                continue
+            pr = oracle.softmax_t(Lref[r], T)
+            C = np.cumsum(pr)
+            uu = float(m.uniforms[r, k])
+            lo = (C[y - 1] if y > 0 else 0.0) / C[-1]
+            hi = C[y] / C[-1]
+            assert pr[y] > 0 and lo - TOL <= uu < hi + TOL, f"step {k} request {r}: token {y} outside CDF bracket"
+        prev = toks[:, k].astype(np.int64)
+    differ = int((toks != kept).sum())
+    return toks, differ
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_markov_tokens_only(lib, T):
+    """Tensor-core shapes with no logits kept: R = 300 (a partial request
+    block), V = 70000 (a partial last tile), rank 256."""
+    m = synth.markov(seed=306, R=300, gamma=3, V=70000, rank=256, temperature=T)
+    _, differ = _markov_tokens_only_check(lib, m, T)
+    assert differ <= 3 + 900 // 50
+
+
+def test_markov_tokens_only_dspark_shape(lib):
+    """R=512, gamma=7, V=129280, rank 256 with no logits kept (the drafting step
+    of a DSpark round whose verification recomputes the draft logits)."""
+    m = synth.markov(seed=5, R=512, gamma=7, V=129280)
+    _, differ = _markov_tokens_only_check(lib, m, 1.0)
+    report("markov R=512 gamma=7 V=129280 tokens only", draws=512 * 7, differing_from_logits_kept_call=differ)
+    assert differ <= 3 + 3584 // 100
+
+
 # --------------------------------------------------------------------------- scheduler
 def _run_sched(lib, conf, sps, B_max=None):
     import torch
