@@ -737,6 +737,59 @@ def run_workload(args):
         desc, launches, kernel = "confidence head: R=512, gamma=7, H=4096, rank 256, V=129280 bf16", 1, "confidence"
         roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                 "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
+    elif w == "dspark_recompute":
+        Rm, Gm, Vm, rank = 512, 7, 129280, 256
+        m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
+        tgt = synth.dspark_target(5, m.U)
+        U, W1, W2, target = bf(m.U), bf(m.W1), bf(m.W2), bf(tgt)
+        anchor, u_m = td(m.anchor, np.int32), td(m.uniforms, np.float32)
+        conf = td(synth.confidences(5, Rm, Gm))
+        sps = td(synth.sps_table(4096))
+        u_v = td(synth.uniform_f32(5, 44, (Rm, Gm + 1, 2)))
+        toks = torch.empty(Rm, Gm, dtype=torch.int32, device=dev)
+        dlog = torch.empty(Rm, Gm, Vm, dtype=torch.bfloat16, device=dev)
+        lengths = torch.empty(Rm, dtype=torch.int32, device=dev)
+        theta = torch.empty(1, dtype=torch.float64, device=dev)
+        acc = torch.empty(Rm, dtype=torch.int32, device=dev)
+        out = torch.empty(Rm, dtype=torch.int32, device=dev)
+        cst = torch.empty(Rm, Gm, dtype=torch.float32, device=dev)
+        nb_m = specv.specv_markov_draft_workspace_size(Rm, Gm, Vm, rank)
+        nb_r = specv.specv_markov_recompute_logits_workspace_size(Rm, Gm)
+        nb_v = specv.specv_verify_chain_workspace_size(Rm, Gm, Vm, specv.SPECV_BF16)
+        ws_m = torch.empty(nb_m, dtype=torch.uint8, device=dev)
+        ws_s = torch.empty(256, dtype=torch.uint8, device=dev)
+        ws_r = torch.empty(nb_r, dtype=torch.uint8, device=dev)
+        ws_v = torch.empty(nb_v, dtype=torch.uint8, device=dev)
+
+        def call():
+            check(specv.specv_markov_draft(U.data_ptr(), W1.data_ptr(), W2.data_ptr(), anchor.data_ptr(),
+                                           u_m.data_ptr(), Rm, Gm, Vm, rank, 1.0, toks.data_ptr(), None,
+                                           specv.SPECV_BF16, ws_m.data_ptr(), nb_m, sp), "specv_markov_draft")
+            check(specv.specv_schedule(conf.data_ptr(), sps.data_ptr(), Rm, Gm, 4096, lengths.data_ptr(),
+                                       theta.data_ptr(), ws_s.data_ptr(), 256, sp), "specv_schedule")
+            check(specv.specv_markov_recompute_logits(U.data_ptr(), W1.data_ptr(), W2.data_ptr(), anchor.data_ptr(),
+                                                      toks.data_ptr(), lengths.data_ptr(), Rm, Gm, Vm, rank,
+                                                      dlog.data_ptr(), ws_r.data_ptr(), nb_r, sp),
+                  "specv_markov_recompute_logits")
+            check(specv.specv_verify_chain(target.data_ptr(), dlog.data_ptr(), specv.SPECV_BF16, toks.data_ptr(),
+                                           lengths.data_ptr(), u_v.data_ptr(), Rm, Gm, Vm, 1.0, acc.data_ptr(),
+                                           out.data_ptr(), cst.data_ptr(), ws_v.data_ptr(), nb_v, sp),
+                  "specv_verify_chain")
+        ms, clocks = _timed(call, flush, args.steps, args.warmup, stream)
+        ell = lengths.cpu().numpy().astype(np.int64)
+        verified = int(ell.sum())
+        live = int(ell.sum())
+        # drafting: U once per step + W2 once; recompute: the live U rows + W2 + the live rows written;
+        # verification: the live target rows + bonus rows and the live draft rows
+        algo = (Gm * Rm * Vm * 2 + rank * Vm * 2) + (live * Vm * 2 + rank * Vm * 2 + live * Vm * 2) + \
+            int(((ell + 1) * Vm * 2 + ell * Vm * 2).sum())
+        units, unit, metric = verified, "positions/s", "DSpark round (draft, schedule, verify): verified draft positions/sec"
+        desc = (f"DSpark round without kept draft logits: Markov head R=512, gamma=7, V=129280, rank 256 (tokens only, "
+                f"bf16 draw precision); scheduler lengths (sum {verified}); the verified rows' draft logits recomputed; "
+                f"chain verification T=1")
+        launches, kernel = 2 * Gm + 1 + 2 + 2, "markov + schedule + recompute + verify (whole round)"
+        roof = {"bound": "hbm", "achieved": algo / (ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                "traffic": None, "peak_source": peak_kind, "kernel": kernel, "algorithmic_bytes_per_launch": algo}
     elif w == "dspark":
         Rm, Gm, Vm, rank = 512, 7, 129280, 256
         m = synth.markov(seed=5, R=Rm, gamma=Gm, V=Vm, rank=rank)
@@ -806,7 +859,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--requests", type=int, default=64, help="R (smaller for profiling captures)")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "greedy", "tv", "tree", "markov", "markov_tokens", "schedule", "schedule_global", "prune", "confidence", "dart", "dspark"])
+                    choices=["chain", "greedy", "tv", "tree", "markov", "markov_tokens", "schedule", "schedule_global", "prune", "confidence", "dart", "dspark", "dspark_recompute"])
     ap.add_argument("--positions", type=int, default=0, help="Markov workload: draft positions (default 7)")
     args = ap.parse_args()
     world = os.environ.get("WORLD_SIZE")

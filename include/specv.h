@@ -11,6 +11,7 @@
  *   specv_verify_tree_greedy  greedy verification of a linearised candidate tree
  *   specv_dart_tree           DART's candidate tree (top-k per offset, beam, node budget)
  *   specv_markov_draft        the DSpark Markov draft head, sampled position by position
+ *   specv_markov_recompute_logits  the draft logits of the verified positions, recomputed
  *   specv_tv_accept           the analytic acceptance c* = 1 - 1/2 ||p_d - p_t||_1
  *   specv_schedule            DSpark's greedy throughput scheduler
  *   specv_schedule_global     its asynchronous global-search form (dynamic top-K)
@@ -278,7 +279,11 @@ SPECV_API specv_status specv_dart_tree(const void* draft_logits, specv_dtype dty
  *   anchor [R] int32, uniforms [R, gamma] float32 (may be NULL at T = 0).
  *   draft_tokens [R, gamma] int32 out (x_1 .. x_gamma).
  *   draft_logits [R, gamma, V] out or NULL: the raw L_k (before temperature)
- *   in logits_out_dtype (SPECV_F32 or SPECV_BF16).
+ *   in logits_out_dtype (SPECV_F32 or SPECV_BF16).  The draw uses L_k in that
+ *   precision (SPECV_BF16: rounded to bfloat16), also when draft_logits is
+ *   NULL; then no logits are written at all (tensor-core form) and
+ *   specv_markov_recompute_logits can later produce the rows a verification
+ *   reads, equal to the ones drawn from.
  *   1 <= rank <= SPECV_MAX_MARKOV_RANK, rank % 16 == 0; V <= 262144 (larger V
  *   returns SPECV_ERR_UNSUPPORTED).
  * Execution: when rank is a multiple of 64 and at most 256, V is a multiple of
@@ -296,6 +301,34 @@ SPECV_API specv_status specv_markov_draft(const void* U, const void* W1, const v
                                 int R, int gamma, int V, int rank, float temperature,
                                 int32_t* draft_tokens, void* draft_logits, specv_dtype logits_out_dtype,
                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * specv_markov_recompute_logits -- the draft logits a chain verification
+ * reads, recomputed after drafting without kept logits ([DSpark guide],
+ * Markov head: L_k = U_k + W1[x_{k-1}] . W2; the verification rule reads
+ * p_k only at the positions that are verified).
+ *   For every request r and k < lengths[r] (all k < gamma when lengths is
+ *   NULL): draft_logits[r, k, :] = L (bf16), with x_{k-1} = anchor[r] for
+ *   k = 0 and draft_tokens[r, k-1] otherwise.  The sums run on the tensor
+ *   cores in the tiling specv_markov_draft uses when it keeps no logits, so
+ *   the rows equal the bf16 logits those draws were taken from.  Other rows of
+ *   draft_logits are not written.
+ *   U [R, gamma, V], W1 [V, rank], W2 [rank, V] bf16; anchor [R],
+ *   draft_tokens [R, gamma], lengths [R] int32 (0 <= lengths[r] <= gamma);
+ *   draft_logits [R, gamma, V] bf16 out.  Workspace of at least
+ *   specv_markov_recompute_logits_workspace_size(R, gamma) bytes.
+ * Shapes: rank a multiple of 64 and at most 256, V a multiple of 8, U, W1, W2
+ *   and draft_logits 16-byte aligned; other shapes give SPECV_ERR_UNSUPPORTED.
+ * Errors: SPECV_ERR_INVALID_ARG for bad sizes or pointers; a length outside
+ *   [0, gamma] counts as 0 and sets SPECV_ERR_DEVICE_DATA; a previous token
+ *   outside [0, V) gives that row W1 = 0.
+ */
+SPECV_API size_t specv_markov_recompute_logits_workspace_size(int R, int gamma);
+SPECV_API specv_status specv_markov_recompute_logits(const void* U, const void* W1, const void* W2,
+                                                     const int32_t* anchor, const int32_t* draft_tokens,
+                                                     const int32_t* lengths, int R, int gamma, int V, int rank,
+                                                     void* draft_logits, void* workspace, size_t workspace_bytes,
+                                                     void* stream);
 
 /* ------------------------------------------------------------------ scheduler */
 

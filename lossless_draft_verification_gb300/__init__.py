@@ -25,13 +25,15 @@ __all__ = [
     "SPECV_ERR_DEVICE_DATA", "SPECV_ERR_TIMEOUT", "SPECV_ERR_SCRATCH_LIMIT", "SPECV_F32", "SPECV_BF16", "EXPORTED",
     "specv_verify_chain_workspace_size", "specv_verify_chain", "specv_verify_chain_noalloc", "specv_tv_accept_workspace_size", "specv_tv_accept",
     "specv_verify_tree_greedy_workspace_size", "specv_verify_tree_greedy", "specv_markov_draft_workspace_size",
-    "specv_markov_draft", "specv_schedule_workspace_size", "specv_schedule", "specv_schedule_global", "specv_prune_threshold",
+    "specv_markov_draft", "specv_markov_recompute_logits_workspace_size", "specv_markov_recompute_logits",
+    "specv_schedule_workspace_size", "specv_schedule", "specv_schedule_global", "specv_prune_threshold",
     "specv_confidence_head_workspace_size", "specv_confidence_head", "specv_dart_tree_workspace_size",
     "specv_dart_tree",
     "specv_read_device_error", "specv_selftest_bounded_wait",
     "specv_status_string", "specv_abi_version", "specv_shard_combine_normalisers", "specv_shard_pick",
     "specv_shard_argmax_combine",
-    "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "schedule", "schedule_global",
+    "verify_chain", "tv_accept", "verify_tree_greedy", "markov_draft", "markov_recompute_logits", "schedule",
+    "schedule_global",
     "prune_threshold", "confidence_head", "dart_tree", "read_device_error",
 ]
 
@@ -58,6 +60,9 @@ EXPORTED = {
     "specv_markov_draft_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "specv_markov_draft": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp,
                                     _c_int, _vp, _c_size, _vp]),
+    "specv_markov_recompute_logits_workspace_size": (_c_size, [_c_int, _c_int]),
+    "specv_markov_recompute_logits": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                               _c_size, _vp]),
     "specv_schedule_workspace_size": (_c_size, [_c_int, _c_int]),
     "specv_schedule": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "specv_schedule_global": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
@@ -157,6 +162,16 @@ def specv_markov_draft(U, W1, W2, anchor, uniforms, R, gamma, V, rank, temperatu
                        logits_out_dtype, workspace, workspace_bytes, stream):
     return _call("specv_markov_draft", U, W1, W2, anchor, uniforms, R, gamma, V, rank, temperature, draft_tokens,
                  draft_logits, logits_out_dtype, workspace, workspace_bytes, stream)
+
+
+def specv_markov_recompute_logits_workspace_size(R, gamma):
+    return _call("specv_markov_recompute_logits_workspace_size", R, gamma)
+
+
+def specv_markov_recompute_logits(U, W1, W2, anchor, draft_tokens, lengths, R, gamma, V, rank, draft_logits, workspace,
+                                  workspace_bytes, stream):
+    return _call("specv_markov_recompute_logits", U, W1, W2, anchor, draft_tokens, lengths, R, gamma, V, rank,
+                 draft_logits, workspace, workspace_bytes, stream)
 
 
 def specv_schedule_workspace_size(R, gamma):
@@ -450,6 +465,31 @@ def markov_draft(U, W1, W2, anchor, uniforms, temperature: float, want_logits: b
                             _p(toks), _p(logits), code, _p(ws), ws.numel(), _stream_ptr(stream))
     _raise(st, "specv_markov_draft")
     return toks, logits
+
+
+def markov_recompute_logits(U, W1, W2, anchor, draft_tokens, lengths=None, out=None, workspace=None, stream=None):
+    """Draft logits of the verified positions (k < lengths[r]) recomputed after
+    drafting without kept logits; returns `out` [R, gamma, V] bf16 (other rows
+    untouched; a new uninitialised tensor when out is None)."""
+    torch = _torch()
+    R, gamma, V = U.shape
+    rank = W1.shape[1]
+    dev = U.device
+    _check(U, "U", dev, torch.bfloat16)
+    _check(W1, "W1", dev, torch.bfloat16, (V, rank))
+    _check(W2, "W2", dev, torch.bfloat16, (rank, V))
+    _check(anchor, "anchor", dev, torch.int32, (R,))
+    _check(draft_tokens, "draft_tokens", dev, torch.int32, (R, gamma))
+    _check(lengths, "lengths", dev, torch.int32, (R,))
+    if out is None:
+        out = torch.empty(R, gamma, V, dtype=torch.bfloat16, device=dev)
+    _check(out, "out", dev, torch.bfloat16, (R, gamma, V))
+    nbytes = specv_markov_recompute_logits_workspace_size(R, gamma)
+    ws = _workspace(nbytes, dev, workspace)
+    st = specv_markov_recompute_logits(_p(U), _p(W1), _p(W2), _p(anchor), _p(draft_tokens), _p(lengths), R, gamma, V,
+                                       rank, _p(out), _p(ws), ws.numel(), _stream_ptr(stream))
+    _raise(st, "specv_markov_recompute_logits")
+    return out
 
 
 def schedule(conf, sps, B_max: int | None = None, workspace=None, stream=None):

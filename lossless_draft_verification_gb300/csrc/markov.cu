@@ -342,9 +342,11 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     __syncthreads();
     if (threadIdx.x < 64) {
       float x = neg_inf();
-      if (!bad && v < a.V)
+      if (!bad && v < a.V) {
         x = bf16_to_f32(a.U[(size_t(r) * a.gamma + (a.k - 1)) * a.V + v]) +
             ((s_chunk[0][c] + s_chunk[1][c]) + (s_chunk[2][c] + s_chunk[3][c]));
+        if (a.logits_bf16) x = round_to_bf16(x);
+      }
       s_chunk[0][c] = x;                       // the tile's logits, in column order
     }
     __syncthreads();
@@ -581,10 +583,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4*>(urow + sw128(rl, c));
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar_tempty[g]);
-        mbar_arrive(&bar_uempty[us]);
-      }
+      if (lane == 0) mbar_arrive(&bar_tempty[g]);
       // L = U + acc, two columns per packed add
       float L[64];
 #pragma unroll
@@ -604,6 +603,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           L[j + 1] = x.y;
         }
       }
+      // release the U stage only after the adds above consumed its values
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_uempty[us]);
       if (n0 + 64 > a.V) {                          // the last tile: columns past V read -inf
 #pragma unroll
         for (int j = 0; j < 64; ++j)
@@ -686,6 +688,574 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
 }
 
+// ---------------------------------------------------------------------------
+// Wide tensor-core form for drafting without kept logits: N = 256 columns per
+// MMA.  At N = 64 each tcgen05.mma re-reads a 4 KB slice of the A operand from
+// shared memory for 2 KB of B, and the operand reads bound the tensor core;
+// at N = 256 one A read serves four times the columns.
+//   W2 ring: stages of one 64-row rank chunk of a 256-column tile (four 8 KB
+//            TMA boxes, 32 KB), filled by the W2 TMA warp;
+//   U rings: one per epilogue group, two 64-column chunks of U (16 KB
+//            each), each filled by its own TMA warp, so U never waits behind
+//            W2.  A ring is waited on only by the group that empties it, so a
+//            waiter is never two phases ahead of a slot (a parity wait cannot
+//            tell phase n from phase n + 2);
+//   MMA:     four K = 16 instructions per rank chunk into one of two
+//            256-column TMEM accumulators;
+//   epilogue: two groups of four warps alternate tiles; each reads its
+//            accumulator in four 64-column chunks, adds U and writes the
+//            64-column tile partials the sampler combines (tile_w = 64).
+constexpr int kWN = 256;                  // columns per tile (UMMA N)
+constexpr int kWChunks = kWN / 64;        // 64-column chunks per tile
+constexpr int kWStagesB = 3;              // W2 ring: rank chunks
+constexpr int kWStagesU = 2;              // U ring per epilogue group: 64-column chunks
+constexpr int kWThreads = (kTcEpiWarps + 4) * 32;    // + W2 TMA, two U TMA, MMA warps
+constexpr uint32_t kWTmemCols = 512;      // two accumulator buffers of 256 columns
+constexpr size_t kWStageB = size_t(kWChunks) * 64 * kTcRowBytes;       // 32 KB
+constexpr size_t kWStageU = size_t(kTcBM) * kTcRowBytes;               // 16 KB
+constexpr size_t kWSmem = kTcSmemE + kWStagesB * kWStageB + 2 * kWStagesU * kWStageU + 1024;
+constexpr uint32_t kWIdesc = tc::idesc_bf16_f32(kTcBM, kWN, true);     // B = W2, MN-major
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    markov_tcw_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
+                      MarkovTcArgs ta) {
+  const MarkovArgs& a = ta.m;
+  extern __shared__ uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kWStagesB], bar_empty[kWStagesB], bar_ufull[2][kWStagesU],
+      bar_uempty[2][kWStagesU], bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_err;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
+  uint8_t* sB = sE + kTcSmemE;                      // [stage][column block][64 k-rows][128 B]
+  uint8_t* sU = sB + kWStagesB * kWStageB;          // [group][stage][128 rows][128 B]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mb = blockIdx.x / ta.per_mb, j0 = blockIdx.x - (blockIdx.x / ta.per_mb) * ta.per_mb;
+  const int row0 = mb * kTcBM;
+  const int nwt = (ta.ntiles + kWChunks - 1) / kWChunks;       // 256-column tiles
+  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWStagesB; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    for (int g = 0; g < 2; ++g)
+      for (int i = 0; i < kWStagesU; ++i) {
+        mbar_init(&bar_ufull[g][i], 1);
+        mbar_init(&bar_uempty[g][i], 4);
+      }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 4);
+    }
+    mbar_init(&bar_done, 1);
+    s_err = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcEpiWarps + 3) tc::tmem_alloc(&s_tmem, kWTmemCols);
+  pdl_wait_primary();                      // the previous step's tokens are complete
+  if (warp < kTcEpiWarps) {
+    // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
+    for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
+      const int req = row0 + r;
+      int x = -1;
+      if (req < a.R) {
+        x = prev_token(a, req);
+        if (x < 0 || x >= a.V) x = -1;
+      }
+      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
+      for (int kc = 0; kc < ta.nkc; ++kc) {
+        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(dst + sw128(r, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kTcEpiWarps) {
+    // ---- W2 producer: one stage per (tile, rank chunk), four 64-column boxes
+    if (lane == 0) {
+      const uint64_t keep = tc::policy_evict_last();
+      int q = 0;                                   // (tile, chunk) sequence number
+      for (int t = j0; t < nwt; t += ta.per_mb)
+        for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
+          const int s = q % kWStagesB;
+          if (!mbar_wait_parity(&bar_empty[s], ((q / kWStagesB) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
+          mbar_arrive_expect_tx(&bar_full[s], uint32_t(kWStageB));
+          for (int b = 0; b < kWChunks; ++b)
+            tc::tma_load_2d_hint(sB + size_t(s) * kWStageB + size_t(b) * (64 * kTcRowBytes), &tmap_w2,
+                                 t * kWN + b * 64, kc * 64, &bar_full[s], keep);
+        }
+      for (int d = (q >= kWStagesB ? q - kWStagesB : 0); d < q; ++d)   // issued copies have landed
+        if (!mbar_wait_parity(&bar_full[d % kWStagesB], (d / kWStagesB) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 1 || warp == kTcEpiWarps + 2) {
+    // ---- U producer of epilogue group g: 64-column chunks of U_k for its tiles
+    const int g = warp - (kTcEpiWarps + 1);
+    if (lane == 0) {
+      const uint64_t once = tc::policy_evict_first();
+      uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+      int q = 0;                                   // chunk sequence number within the group
+      for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb)
+        for (int c = 0; c < kWChunks; ++c, ++q) {
+          const int s = q % kWStagesU;
+          if (!mbar_wait_parity(&bar_uempty[g][s], ((q / kWStagesU) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
+          mbar_arrive_expect_tx(&bar_ufull[g][s], uint32_t(kWStageU));
+          tc::tma_load_3d_hint(ring + size_t(s) * kWStageU, &tmap_u, t * kWN + c * 64, a.k - 1, row0,
+                               &bar_ufull[g][s], once);
+        }
+      for (int d = (q >= kWStagesU ? q - kWStagesU : 0); d < q; ++d)
+        if (!mbar_wait_parity(&bar_ufull[g][d % kWStagesU], (d / kWStagesU) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 3) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      const uint64_t da0 = tc::smem_desc_k_sw128(smem_addr(sE));
+      uint64_t db0[kWStagesB];
+#pragma unroll
+      for (int st = 0; st < kWStagesB; ++st)
+        db0[st] = tc::smem_desc_mn_sw128(smem_addr(sB) + uint32_t(st) * uint32_t(kWStageB), 1024, 64 * kTcRowBytes);
+      int q = 0, i = 0;
+      bool ok = true;
+      for (int t = j0; t < nwt && ok; t += ta.per_mb, ++i) {
+        const int tb = i & 1;
+        if (!mbar_wait_parity(&bar_tempty[tb], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t dtm = tmem + uint32_t(tb * kWN);
+        for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
+          const int s = q % kWStagesB;
+          if (!mbar_wait_parity(&bar_full[s], (q / kWStagesB) & 1, kTcMaxPolls)) { s_err = 1; ok = false; break; }
+          tc::fence_after_sync();
+          uint64_t dbs = db0[0];
+#pragma unroll
+          for (int st = 1; st < kWStagesB; ++st)
+            if (s == st) dbs = db0[st];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: chunk kc (16 KB apart), 32-byte K step; B: 16 k-rows = two 1024-byte groups
+            const uint64_t da = da0 + uint64_t(kc * (kTcBM * kTcRowBytes / 16) + kk * 2);
+            const uint64_t db = dbs + uint64_t(kk * (2048 / 16));
+            tc::mma_bf16(dtm, da, db, kWIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(&bar_empty[s]);          // the W2 stage is free once these MMAs have read it
+        }
+        if (ok) tc::commit(&bar_tfull[tb]);   // the accumulator is ready for the epilogue
+      }
+      tc::commit(&bar_done);
+      if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
+    }
+  } else {
+    // ---- epilogue group g = warp / 4 takes tiles i = g, g + 2, ...; thread = request row
+    const int g = warp >> 2, qd = warp & 3;
+    const int rl = qd * 32 + lane;
+    const int r = row0 + rl;
+    const bool rv = r < a.R;
+    uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+    int i = g;
+    for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb, i += 2) {
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], (i >> 1) & 1, kTcMaxPolls))) {
+        s_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int c = 0; c < kWChunks; ++c) {
+        const int q = (i >> 1) * kWChunks + c, us = q % kWStagesU;   // this group's chunk sequence
+        float acc0[32], acc1[32];
+        const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(g * kWN + c * 64);
+        tc::tmem_ld32(taddr, acc0);
+        tc::tmem_ld32(taddr + 32, acc1);
+        tc::tmem_ld_wait();
+        if (c == kWChunks - 1) {               // the accumulator has been read
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_tempty[g]);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_ufull[g][us], (q / kWStagesU) & 1, kTcMaxPolls))) {
+          s_err = 1;
+          ok = false;
+          break;
+        }
+        uint4 u[8];
+        const uint8_t* urow = ring + size_t(us) * kWStageU;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4*>(urow + sw128(rl, cc));
+        const int n0 = t * kWN + c * 64;
+        float L[64];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t wv[4] = {u[cc].x, u[cc].y, u[cc].z, u[cc].w};
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int j = 8 * cc + e;
+            const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
+            const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
+            float2 x = add2(ub, ac);
+            if (a.logits_bf16) {                  // the draw uses the logits rounded to bf16
+              x.x = round_to_bf16(x.x);
+              x.y = round_to_bf16(x.y);
+            }
+            L[j] = x.x;
+            L[j + 1] = x.y;
+          }
+        }
+        // The slot is released only now: the adds above consumed every value
+        // read from it, so no read can still be outstanding when the copy of a
+        // later chunk overwrites it.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_uempty[g][us]);
+        if (n0 + 64 > a.V) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (n0 + j >= a.V) L[j] = neg_inf();
+        }
+        if (!rv || n0 >= a.V) continue;
+        MarkovPart mpart;
+        if (a.greedy) {
+          float m = L[0];
+          int idx = n0;
+#pragma unroll
+          for (int j = 1; j < 64; ++j)
+            if (L[j] > m) { m = L[j]; idx = n0 + j; }
+          mpart.a = m;
+          mpart.b = __int_as_float(idx);
+        } else {
+          float mx[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(L[j], L[j + 16]), fmaxf(L[j + 32], L[j + 48]));
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+          const float m_c2 = mx[0] * a.c2;
+          const float2 c2v = make_float2(a.c2, a.c2), mv = make_float2(-m_c2, -m_c2);
+          float2 z[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float2 tt = fma2(make_float2(L[j], L[j + 1]), c2v, mv);
+            z[(j >> 1) & 3] = add2(z[(j >> 1) & 3], make_float2(ex2(tt.x), ex2(tt.y)));
+          }
+          mpart.a = m_c2;
+          mpart.b = ((z[0].x + z[0].y) + (z[1].x + z[1].y)) + ((z[2].x + z[2].y) + (z[3].x + z[3].y));
+        }
+        a.part[size_t(r) * a.ntile + (n0 >> 6)] = mpart;
+      }
+      if (!ok) break;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kTcEpiWarps + 3) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kWTmemCols);
+  }
+  if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// Recomputing the draft logits a verification reads.  After drafting without
+// kept logits and scheduling, only the rows (r, k) with k < l_r are verified.
+// markov_rows_prep lists them; markov_rows_kernel recomputes
+// L = U[r, k] + W1[x_{k-1}] . W2 for those rows with the same 256-column
+// tensor-core tiling as markov_tcw (so the float32 sums, and their bf16
+// rounding, are the ones the draws used) and writes them as bf16 into the
+// usual [R, gamma, V] layout.  Rows are gathered, so U comes in by 16-byte
+// async copies issued by each epilogue warp for its own 32 rows, two chunks
+// ahead, rather than by a TMA box; the logits leave the same way.
+constexpr int kRowsListOff = 64;          // workspace header: int32 live-row count at this byte offset
+constexpr int kRowsUStages = 2;           // U chunks in flight per epilogue group
+constexpr size_t kRowsSmem = kTcSmemE + kWStagesB * kWStageB + size_t(2) * kRowsUStages * kWStageU + 1024;
+
+struct RowsArgs {
+  const uint16_t* U;
+  const uint16_t* W1;
+  const int32_t* anchor;
+  const int32_t* tokens;      // [R, gamma]
+  const int32_t* lengths;     // [R] or null (gamma)
+  uint16_t* out;              // [R, gamma, V] bf16
+  int32_t* rows;              // [R * gamma]: r * gamma + k of each live row, in (r, k) order
+  void* workspace;
+  int R, gamma, V, rank, nkc;
+  int ntiles;                 // 256-column tiles
+};
+
+// one CTA: prefix over the lengths, then the list of live rows
+__global__ void __launch_bounds__(1024) markov_rows_prep(RowsArgs a) {
+  __shared__ int s_warp[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (a.R + 1023) / 1024;
+  const int r0 = threadIdx.x * per, r1 = min(a.R, r0 + per);
+  int cnt = 0;
+  bool bad = false;
+  for (int r = r0; r < r1; ++r) {
+    int l = a.lengths ? a.lengths[r] : a.gamma;
+    if (l < 0 || l > a.gamma) { l = 0; bad = true; }
+    cnt += l;
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int wpre = 0, total = 0;
+  for (int w = 0; w < 32; ++w) {
+    if (w < warp) wpre += s_warp[w];
+    total += s_warp[w];
+  }
+  int off = wpre + incl - cnt;
+  for (int r = r0; r < r1; ++r) {
+    int l = a.lengths ? a.lengths[r] : a.gamma;
+    if (l < 0 || l > a.gamma) l = 0;
+    for (int k = 0; k < l; ++k) a.rows[off + k] = r * a.gamma + k;
+    off += l;
+  }
+  if (threadIdx.x == 0) {
+    *reinterpret_cast<int*>(a.workspace) = 0;
+    reinterpret_cast<int*>(a.workspace)[kRowsListOff / 4] = total;
+  }
+  __syncthreads();
+  if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
+  pdl_launch_dependents();
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    markov_rows_kernel(const __grid_constant__ CUtensorMap tmap_w2, RowsArgs a) {
+  extern __shared__ uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kWStagesB], bar_empty[kWStagesB], bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_err, s_n;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
+  uint8_t* sB = sE + kTcSmemE;                      // [stage][column block][64 k-rows][128 B]
+  uint8_t* sU = sB + kWStagesB * kWStageB;          // [group][stage][128 rows][128 B], each thread its own row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait_primary();                               // the row list is complete
+  if (threadIdx.x == 0) s_n = reinterpret_cast<const int*>(a.workspace)[kRowsListOff / 4];
+  __syncthreads();
+  const int n_rows = s_n;
+  const int n_mb = (n_rows + kTcBM - 1) / kTcBM;
+  if (n_mb == 0) return;                            // block-uniform: nothing to recompute
+  const int per_mb = int(gridDim.x) / n_mb > 0 ? int(gridDim.x) / n_mb : 1;
+  const int mb = int(blockIdx.x) / per_mb, j0 = int(blockIdx.x) - (int(blockIdx.x) / per_mb) * per_mb;
+  if (mb >= n_mb) return;                           // block-uniform: an idle CTA (n_mb * per_mb <= grid)
+  const int row0 = mb * kTcBM;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWStagesB; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 4);
+    }
+    mbar_init(&bar_done, 1);
+    s_err = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kWTmemCols);
+  if (warp < kTcEpiWarps) {
+    // A operand: the previous token of each listed row
+    for (int rl = threadIdx.x; rl < kTcBM; rl += kTcEpiWarps * 32) {
+      int x = -1;
+      if (row0 + rl < n_rows) {
+        const int rk = a.rows[row0 + rl];
+        const int r = rk / a.gamma, k = rk - (rk / a.gamma) * a.gamma;
+        x = k == 0 ? a.anchor[r] : a.tokens[size_t(r) * a.gamma + (k - 1)];
+        if (x < 0 || x >= a.V) x = -1;
+      }
+      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
+      for (int kc = 0; kc < a.nkc; ++kc) {
+        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(dst + sw128(rl, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kTcEpiWarps) {
+    // ---- W2 producer (as in markov_tcw)
+    if (lane == 0) {
+      const uint64_t keep = tc::policy_evict_last();
+      int q = 0;
+      for (int t = j0; t < a.ntiles; t += per_mb)
+        for (int kc = 0; kc < a.nkc; ++kc, ++q) {
+          const int s = q % kWStagesB;
+          if (!mbar_wait_parity(&bar_empty[s], ((q / kWStagesB) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = a.ntiles; break; }
+          mbar_arrive_expect_tx(&bar_full[s], uint32_t(kWStageB));
+          for (int b = 0; b < kWChunks; ++b)
+            tc::tma_load_2d_hint(sB + size_t(s) * kWStageB + size_t(b) * (64 * kTcRowBytes), &tmap_w2,
+                                 t * kWN + b * 64, kc * 64, &bar_full[s], keep);
+        }
+      for (int d = (q >= kWStagesB ? q - kWStagesB : 0); d < q; ++d)
+        if (!mbar_wait_parity(&bar_full[d % kWStagesB], (d / kWStagesB) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 1) {
+    // ---- MMA issuer (as in markov_tcw)
+    if (lane == 0) {
+      const uint64_t da0 = tc::smem_desc_k_sw128(smem_addr(sE));
+      uint64_t db0[kWStagesB];
+#pragma unroll
+      for (int st = 0; st < kWStagesB; ++st)
+        db0[st] = tc::smem_desc_mn_sw128(smem_addr(sB) + uint32_t(st) * uint32_t(kWStageB), 1024, 64 * kTcRowBytes);
+      int q = 0, i = 0;
+      bool ok = true;
+      for (int t = j0; t < a.ntiles && ok; t += per_mb, ++i) {
+        const int tb = i & 1;
+        if (!mbar_wait_parity(&bar_tempty[tb], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t dtm = tmem + uint32_t(tb * kWN);
+        for (int kc = 0; kc < a.nkc; ++kc, ++q) {
+          const int s = q % kWStagesB;
+          if (!mbar_wait_parity(&bar_full[s], (q / kWStagesB) & 1, kTcMaxPolls)) { s_err = 1; ok = false; break; }
+          tc::fence_after_sync();
+          uint64_t dbs = db0[0];
+#pragma unroll
+          for (int st = 1; st < kWStagesB; ++st)
+            if (s == st) dbs = db0[st];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = da0 + uint64_t(kc * (kTcBM * kTcRowBytes / 16) + kk * 2);
+            const uint64_t db = dbs + uint64_t(kk * (2048 / 16));
+            tc::mma_bf16(dtm, da, db, kWIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(&bar_empty[s]);
+        }
+        if (ok) tc::commit(&bar_tfull[tb]);
+      }
+      tc::commit(&bar_done);
+      if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
+    }
+  } else {
+    // ---- epilogue group g takes tiles i = g, g + 2, ...; thread = listed row.
+    // A warp moves its 32 rows' chunks cooperatively: in each 16-byte copy or
+    // store instruction lane l takes granule l % 8 of row 4m + l / 8, so one
+    // instruction covers four whole 128-byte row pieces instead of 32
+    // scattered granules.  The warp's staging holds row j's granule q at
+    // granule q ^ (j % 8) (conflict-free both ways); each thread reads its own
+    // row from it, and the bf16 logits go back through it to be stored.
+    const int g = warp >> 2, qd = warp & 3;
+    const int rl = qd * 32 + lane;
+    const bool rv = row0 + rl < n_rows;
+    int rk = 0;
+    if (rv) rk = a.rows[row0 + rl];
+    const int gq = lane & 7;                           // granule this lane moves
+    int rks[8];                                        // rows 4m + lane / 8 of this warp
+    bool vld[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int jr = 4 * m + (lane >> 3);
+      rks[m] = __shfl_sync(0xffffffffu, rk, jr);
+      vld[m] = row0 + qd * 32 + jr < n_rows;
+    }
+    uint8_t* wstage = sU + size_t(g * kRowsUStages) * kWStageU + size_t(qd) * 32 * kTcRowBytes;   // + stage * kWStageU
+    // this group's chunk sequence: n = (tile index within the group) * 4 + c
+    const int n_tiles_g = (a.ntiles - (j0 + g * per_mb) + 2 * per_mb - 1) / (2 * per_mb);
+    const int n_chunks = n_tiles_g > 0 ? n_tiles_g * kWChunks : 0;
+    auto col_of = [&](int n) { return (j0 + g * per_mb + (n / kWChunks) * 2 * per_mb) * kWN + (n % kWChunks) * 64; };
+    auto issue = [&](int n) {                      // copy chunk n of the warp's rows into stage n % 2
+      if (n < n_chunks) {
+        const int c0 = col_of(n) + gq * 8;
+        uint8_t* st = wstage + size_t(n % kRowsUStages) * kWStageU;
+        if (c0 < a.V) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int jr = 4 * m + (lane >> 3);
+            if (vld[m]) cp_async16(st + jr * kTcRowBytes + ((gq ^ (jr & 7)) << 4), a.U + size_t(rks[m]) * a.V + c0);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+    issue(0);
+    issue(1);
+    int n = 0, i = g;
+    for (int t = j0 + g * per_mb; t < a.ntiles; t += 2 * per_mb, i += 2) {
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], (i >> 1) & 1, kTcMaxPolls))) {
+        s_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      for (int c = 0; c < kWChunks; ++c, ++n) {
+        float acc0[32], acc1[32];
+        const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(g * kWN + c * 64);
+        tc::tmem_ld32(taddr, acc0);
+        tc::tmem_ld32(taddr + 32, acc1);
+        tc::tmem_ld_wait();
+        if (c == kWChunks - 1) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_tempty[g]);
+        }
+        cp_async_wait_group<1>();                   // this lane's copies of chunk n have landed
+        __syncwarp();                               // ... and every other lane's
+        uint8_t* st = wstage + size_t(n % kRowsUStages) * kWStageU;
+        uint8_t* mine = st + lane * kTcRowBytes;
+        uint4 u[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4*>(mine + ((cc ^ (lane & 7)) << 4));
+        const int n0 = t * kWN + c * 64;
+        uint4 o[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t wv[4] = {u[cc].x, u[cc].y, u[cc].z, u[cc].w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int j = 8 * cc + e;
+            const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
+            const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
+            const float2 x = add2(ub, ac);
+            ow[e >> 1] = (__float_as_uint(round_to_bf16(x.x)) >> 16) | (__float_as_uint(round_to_bf16(x.y)) & 0xFFFF0000u);
+          }
+          o[cc] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        __syncwarp();                               // every lane has read its U row
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(mine + ((cc ^ (lane & 7)) << 4)) = o[cc];
+        __syncwarp();                               // the warp's logits are staged
+        if (n0 + gq * 8 < a.V) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int jr = 4 * m + (lane >> 3);
+            const uint4 v = *reinterpret_cast<const uint4*>(st + jr * kTcRowBytes + ((gq ^ (jr & 7)) << 4));
+            if (vld[m]) *reinterpret_cast<uint4*>(a.out + size_t(rks[m]) * a.V + n0 + gq * 8) = v;
+          }
+        }
+        __syncwarp();                               // the staging is read: refill it
+        issue(n + 2);
+      }
+    }
+    cp_async_wait_all();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kTcEpiWarps + 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kWTmemCols);
+  }
+  if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+}
+
 namespace {
 // Workspace: header | tile partials [R, ceil(V / 64)] | float32 logits [R, V]
 // (when the caller keeps none)
@@ -715,6 +1285,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     fn.store(p, std::memory_order_release);
   }
   return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+}
+
+// W2 [rank, V] bf16 as [64-column x 64-row] 128-byte-swizzled boxes
+bool encode_w2(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, const void* W2, int rank, int V) {
+  const cuuint64_t gdim[2] = {cuuint64_t(V), cuuint64_t(rank)};
+  const cuuint64_t gstride[1] = {cuuint64_t(V) * 2};
+  const cuuint32_t box[2] = {uint32_t(kTcBN), 64};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), gdim, gstride, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -775,8 +1356,8 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     a.logits_bf16 = logits_out_dtype == SPECV_BF16;
     a.lstride_r = long(gamma) * V;
   } else {
-    a.logits = base + L.scratch_off;            // [R, V] float32, reused by every step (CUDA-core form)
-    a.logits_bf16 = 0;
+    a.logits = base + L.scratch_off;            // [R, V], reused by every step (CUDA-core form)
+    a.logits_bf16 = logits_out_dtype == SPECV_BF16;   // the precision the draw uses
     a.lstride_r = V;
   }
   a.part = reinterpret_cast<MarkovPart*>(base + L.part_off);
@@ -797,16 +1378,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     const long slots = draft_logits ? gamma : 1;
     const bool lbf = a.logits_bf16 != 0;
     CUtensorMap tmap_w2, tmap_u, tmap_l;
-    {
-      const cuuint64_t gdim[2] = {cuuint64_t(V), cuuint64_t(rank)};
-      const cuuint64_t gstride[1] = {cuuint64_t(V) * 2};
-      const cuuint32_t box[2] = {uint32_t(kTcBN), 64};
-      const cuuint32_t es[2] = {1, 1};
-      if (encode(&tmap_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), gdim, gstride, box, es,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return SPECV_ERR_CUDA;
-    }
+    if (!encode_w2(encode, &tmap_w2, W2, rank, V)) return SPECV_ERR_CUDA;
     {
       const cuuint64_t gdim[3] = {cuuint64_t(V), cuuint64_t(gamma), cuuint64_t(R)};
       const cuuint64_t gstride[2] = {cuuint64_t(V) * 2, cuuint64_t(gamma) * V * 2};
@@ -828,10 +1400,11 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SPECV_ERR_CUDA;
     }
-    // three-stage rings when no logits are staged for storing, else two
+    // Logits kept: the 64-column kernel stages and stores them.  None kept: the
+    // 256-column kernel, which writes only the tile partials.
     const bool store = draft_logits != nullptr;
-    void* tc_fn = store ? reinterpret_cast<void*>(&markov_tc_kernel<2>) : reinterpret_cast<void*>(&markov_tc_kernel<3>);
-    const size_t tc_bytes = store ? tc_smem(2, true) : tc_smem(3, false);
+    void* tc_fn = store ? reinterpret_cast<void*>(&markov_tc_kernel<2>) : reinterpret_cast<void*>(&markov_tcw_kernel);
+    const size_t tc_bytes = store ? tc_smem(2, true) : kWSmem;
     if (cudaFuncSetAttribute(tc_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tc_bytes)) != cudaSuccess)
       return SPECV_ERR_CUDA;
     MarkovTcArgs ta;
@@ -860,10 +1433,11 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       cfg.attrs = at;
       cfg.numAttrs = 1;
       void* targs[] = {&tmap_w2, &tmap_u, &tmap_l, &ta};
+      void* wargs[] = {&tmap_w2, &tmap_u, &ta};
       cfg.gridDim = g1;
-      cfg.blockDim = dim3(kTcThreads);
+      cfg.blockDim = dim3(store ? kTcThreads : kWThreads);
       cfg.dynamicSmemBytes = tc_bytes;
-      if (cudaLaunchKernelExC(&cfg, tc_fn, targs) != cudaSuccess)
+      if (cudaLaunchKernelExC(&cfg, tc_fn, store ? targs : wargs) != cudaSuccess)
         return SPECV_ERR_CUDA;
       void* sargs[] = {&a};
       cfg.gridDim = dim3(unsigned(R));
@@ -888,5 +1462,62 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
                          0, st) != cudaSuccess)
       return SPECV_ERR_CUDA;
   }
+  return SPECV_OK;
+}
+
+extern "C" size_t specv_markov_recompute_logits_workspace_size(int R, int gamma) {
+  if (R < 0 || gamma < 0 || gamma > SPECV_MAX_GAMMA) return 0;
+  return kHeaderBytes + align256(size_t(R) * gamma * sizeof(int32_t));
+}
+
+extern "C" specv_status specv_markov_recompute_logits(const void* U, const void* W1, const void* W2,
+                                                      const int32_t* anchor, const int32_t* draft_tokens,
+                                                      const int32_t* lengths, int R, int gamma, int V, int rank,
+                                                      void* draft_logits, void* workspace, size_t workspace_bytes,
+                                                      void* stream) {
+  if (R < 0 || gamma < 0 || gamma > SPECV_MAX_GAMMA || V < 1 || rank < 1) return SPECV_ERR_INVALID_ARG;
+  if (R == 0 || gamma == 0) return SPECV_OK;
+  if (!U || !W1 || !W2 || !anchor || !draft_tokens || !draft_logits || !workspace) return SPECV_ERR_INVALID_ARG;
+  if (!aligned_to(anchor, 4) || !aligned_to(draft_tokens, 4) || !aligned_to(lengths, 4) ||
+      !aligned_to(workspace, 256))
+    return SPECV_ERR_INVALID_ARG;
+  if (workspace_bytes < specv_markov_recompute_logits_workspace_size(R, gamma)) return SPECV_ERR_INVALID_ARG;
+  // the tensor-core tiling of drafting without kept logits, whose sums this reproduces
+  if (rank % 64 != 0 || rank > kTcMaxKC * 64 || V % 8 != 0 || !aligned_to(U, 16) || !aligned_to(W1, 16) ||
+      !aligned_to(W2, 16) || !aligned_to(draft_logits, 16))
+    return SPECV_ERR_UNSUPPORTED;
+  specv_status s = check_device();
+  if (s != SPECV_OK) return s;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  const int nsm = sm_count();
+  if (encode == nullptr || nsm < 1) return SPECV_ERR_CUDA;
+  CUtensorMap tmap_w2;
+  if (!encode_w2(encode, &tmap_w2, W2, rank, V)) return SPECV_ERR_CUDA;
+  RowsArgs ra;
+  ra.U = static_cast<const uint16_t*>(U);
+  ra.W1 = static_cast<const uint16_t*>(W1);
+  ra.anchor = anchor;
+  ra.tokens = draft_tokens;
+  ra.lengths = lengths;
+  ra.out = static_cast<uint16_t*>(draft_logits);
+  ra.rows = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kHeaderBytes);
+  ra.workspace = workspace;
+  ra.R = R;
+  ra.gamma = gamma;
+  ra.V = V;
+  ra.rank = rank;
+  ra.nkc = rank / 64;
+  ra.ntiles = (V + kWN - 1) / kWN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* pargs[] = {&ra};
+  if (cudaLaunchKernel(reinterpret_cast<void*>(&markov_rows_prep), dim3(1), dim3(1024), pargs, 0, st) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  if (cudaFuncSetAttribute(reinterpret_cast<void*>(&markov_rows_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kRowsSmem)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
+  void* rargs[] = {&tmap_w2, &ra};
+  if (launch_dependent(reinterpret_cast<void*>(&markov_rows_kernel), dim3(unsigned(nsm)), dim3(kTcThreads), rargs, st,
+                       kRowsSmem) != cudaSuccess)
+    return SPECV_ERR_CUDA;
   return SPECV_OK;
 }

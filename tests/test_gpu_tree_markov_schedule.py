@@ -241,6 +241,130 @@ def test_markov_tokens_only_dspark_shape(lib):
     assert differ <= 3 + 3584 // 100
 
 
+def _recompute_case(lib, m, lengths, T=1.0):
+    """Draft with no kept logits (bf16 draw precision), then recompute the
+    verified rows.  Returns (tokens, recomputed bf16 logits as float64 [R, gamma, V]
+    with NaN in rows that must stay unwritten, the sentinel-filled tensor)."""
+    import torch
+    dev = torch.device("cuda")
+    U, W1, W2 = to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev)
+    anchor = to_torch(m.anchor, dev, np.int32)
+    toks, _ = lib.markov_draft(U, W1, W2, anchor, to_torch(m.uniforms, dev, np.float32), T, False, torch.bfloat16)
+    R, G, V = m.U.shape
+    out = torch.full((R, G, V), 7.0, dtype=torch.bfloat16, device=dev)   # sentinel for rows not written
+    lib.markov_recompute_logits(U, W1, W2, anchor, toks, to_torch(lengths, dev, np.int32), out=out)
+    return toks.cpu().numpy(), out
+
+
+def _check_recomputed_rows(m, toks, out, lengths, T=1.0):
+    """Every listed row within the float32-accumulation + bf16-rounding bound of
+    the oracle's L (conditioned on the GPU's tokens); every other row untouched;
+    each drafted token inside the CDF bracket of its recomputed row (the draw
+    used those logits)."""
+    import torch
+    R, G, V = m.U.shape
+    W164, W264 = m.W1.f64, m.W2.f64
+    rank = W164.shape[1]
+    for k in range(G):
+        prev = (m.anchor if k == 0 else toks[:, k - 1]).astype(np.int64)
+        Lk = out[:, k].float().cpu().numpy().astype(np.float64)
+        live = k < lengths
+        assert (Lk[~live] == 7.0).all(), f"position {k}: a row past its length was written"
+        if not live.any():
+            continue
+        U_k = synth.bf16_bits_to_f64(m.U.raw[live, k])
+        Lref, _, _, _ = oracle.markov_step(U_k, W164, W264, prev[live], m.uniforms[live, k], 1.0)
+        bound = 1e-6 * (1 + np.abs(Lref)) + rank * 2.0 ** -24 * (np.abs(W164[prev[live]]) @ np.abs(W264)) \
+            + np.abs(Lref) * 2.0 ** -8
+        assert (np.abs(Lk[live] - Lref) <= bound).all(), f"position {k}: recomputed logits differ"
+        for i, r in enumerate(np.nonzero(live)[0]):
+            pr = oracle.softmax_t(Lk[r], T)
+            C = np.cumsum(pr)
+            y, uu = int(toks[r, k]), float(m.uniforms[r, k])
+            lo = (C[y - 1] if y > 0 else 0.0) / C[-1]
+            assert pr[y] > 0 and lo - TOL <= uu < C[y] / C[-1] + TOL, f"({r}, {k}): token outside the recomputed CDF"
+
+
+def test_markov_recompute_logits_ragged_lengths(lib):
+    """Verified rows only (ragged lengths, l_r = 0 and l_r = gamma included),
+    R = 300 (a partial 128-row block of listed rows), V = 70000 (a partial last
+    256-column tile)."""
+    m = synth.markov(seed=307, R=300, gamma=4, V=70000, rank=256)
+    lengths = (synth.uniform_u24(307, 9, (300,)) * 5).astype(np.int32)
+    lengths[:3] = [0, 4, 1]
+    toks, out = _recompute_case(lib, m, lengths)
+    _check_recomputed_rows(m, toks, out, lengths)
+
+
+def test_markov_recompute_logits_equal_the_kept_logits(lib):
+    """The recomputed rows against the logits specv_markov_draft keeps when asked
+    (bf16), on the same tokens: the float32 sums may differ only in their
+    order-dependent last bits, so the bf16 values agree except at rounding ties
+    of those bits (counted)."""
+    import torch
+    dev = torch.device("cuda")
+    m = synth.markov(seed=308, R=256, gamma=3, V=129280, rank=256)
+    lengths = np.full(256, 3, dtype=np.int32)
+    toks, out = _recompute_case(lib, m, lengths)
+    kept_toks, kept = lib.markov_draft(to_torch(m.U, dev), to_torch(m.W1, dev), to_torch(m.W2, dev),
+                                       to_torch(m.anchor, dev, np.int32), to_torch(m.uniforms, dev, np.float32), 1.0,
+                                       True, torch.bfloat16)
+    same_tok = (kept_toks.cpu().numpy() == toks)
+    rows = torch.from_numpy(np.nonzero(same_tok.all(1))[0]).to(dev)
+    a = out[rows].view(torch.int16)
+    b = kept[rows].view(torch.int16)
+    differ = int((a != b).sum().item())
+    total = a.numel()
+    report("markov recompute vs kept bf16 logits R=256 gamma=3 V=129280", elements=total, differing_bf16=differ,
+           requests_with_equal_tokens=int(rows.numel()))
+    assert differ <= total // 1000
+
+
+def test_dspark_round_with_recomputed_draft_logits(lib):
+    """The DSpark round without kept draft logits: tokens-only drafting (bf16
+    draw precision) -> scheduler -> the verified rows' draft logits recomputed
+    -> chain verification.  The recomputed rows are checked against the oracle's
+    logits and the verification against oracle.verify_chain on them, request by
+    request (flagged-threshold rule, c* within 1e-5)."""
+    import torch
+    dev = torch.device("cuda")
+    R, G, V = 512, 7, 129280
+    m = synth.markov(seed=5, R=R, gamma=G, V=V)
+    tgt = synth.dspark_target(5, m.U)
+    conf = synth.confidences(5, R, G)
+    sps = synth.sps_table(4096)
+    lengths, _ = lib.schedule(to_torch(conf, dev, np.float32), to_torch(sps, dev, np.float64))
+    ell = lengths.cpu().numpy()
+    assert (ell == oracle.schedule(conf, sps).lengths).all()
+    toks, out = _recompute_case(lib, m, ell)
+    _check_recomputed_rows(m, toks, out, ell)
+    u_np = synth.uniform_f32(5, 44, (R, G + 1, 2))
+    A, y, c = lib.verify_chain(to_torch(tgt, dev), out, to_torch(toks, dev, np.int32), to_torch(u_np, dev, np.float32),
+                               1.0, lengths)
+    A, y, c = A.cpu().numpy(), y.cpu().numpy(), c.cpu().numpy()
+    d_bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    tot = dict(requests=0, exact=0, flagged_accept=0, flagged_sample=0)
+    worst = 0.0
+    for r in range(R):
+        L = int(ell[r])
+        t64 = synth.bf16_bits_to_f64(tgt.raw[r:r + 1, :L + 1])
+        d64 = synth.bf16_bits_to_f64(d_bits[r:r + 1, :L])
+        u = u_np[r:r + 1, :L + 1]
+        res = oracle.verify_chain(t64, d64, toks[r:r + 1, :L].astype(np.int64), u, 1.0)
+        st = check_chain(A[r:r + 1], y[r:r + 1], res, lambda _r, kk: oracle.softmax_t(t64[0, kk], 1.0),
+                         lambda _r, kk: oracle.softmax_t(d64[0, kk], 1.0), u, np.array([L]))
+        for key in ("exact", "flagged_accept", "flagged_sample"):
+            tot[key] += getattr(st, key)
+        tot["requests"] += 1
+        if L:
+            diff = np.abs(c[r, :L] - res.c_star[0])
+            worst = max(worst, float(diff.max()))
+            assert (diff <= TOL).all()
+    report("dspark round with recomputed draft logits R=512 gamma=7 V=129280", sum_l=int(ell.sum()),
+           max_abs_cstar_diff=worst, **tot)
+    assert tot["exact"] >= R - 16
+
+
 # --------------------------------------------------------------------------- scheduler
 def _run_sched(lib, conf, sps, B_max=None):
     import torch
