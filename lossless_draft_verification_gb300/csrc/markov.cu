@@ -193,7 +193,8 @@ constexpr int kSampleMaxRank = 256;   // rank of the tensor-core form, whose til
 
 __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArgs a) {
   __shared__ float s_e[kSampleMaxRank];  // W1[x_{k-1}] when the tile is recomputed
-  __shared__ float s_chunk[4][64];       // per-rank-chunk sums, then the recomputed tile
+  __shared__ float s_wsum[kSampleWarps][64];   // per-warp rank sums of the recomputed tile
+  __shared__ float s_chunk[1][64];       // the recomputed tile
   __shared__ float s_f[kSampleWarps];
   __shared__ int s_i[kSampleWarps];
   __shared__ int s_sel;
@@ -319,32 +320,38 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
   bool bad = bad_in || sel < 0;
   if (a.logits == nullptr) {
     // No logits were kept (tensor-core form, tile_w = 64): recompute the
-    // selected tile's 64 logits, L(v) = U_k(v) + sum_j W1[x_{k-1}, j] W2[j, v],
-    // float32 products summed in four rank chunks (one per group of 64
-    // threads), then the chunks in order.
+    // selected tile's 64 logits, L(v) = U_k(v) + sum_j W1[x_{k-1}, j] W2[j, v].
+    // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
+    // 4-byte load per row, all independent; the warps' float32 sums are then
+    // added in warp order.
     if (!bad)
       for (int j = threadIdx.x; j < a.rank; j += kSampleThreads)
         s_e[j] = bf16_to_f32(a.W1[size_t(x_prev) * a.rank + j]);
     __syncthreads();
-    const int c = threadIdx.x & 63, q = threadIdx.x >> 6;
-    const int v = sel * 64 + c;
-    if (!bad && v < a.V) {
-      const int j0 = q * (a.rank >> 2), j1 = j0 + (a.rank >> 2);
-      const uint16_t* w2 = a.W2 + v;
-      float acc0 = 0.f, acc1 = 0.f;
+    const int v2 = sel * 64 + 2 * lane;                  // this lane's column pair
+    const int per_w = (a.rank + kSampleWarps - 1) / kSampleWarps;
+    float2 acc = make_float2(0.f, 0.f);
+    if (!bad && v2 < a.V) {
+      const int j0 = warp * per_w, j1 = min(a.rank, j0 + per_w);
+      const uint16_t* w2 = a.W2 + v2;
 #pragma unroll 8
-      for (int j = j0; j < j1; j += 2) {
-        acc0 = fmaf(s_e[j], bf16_to_f32(w2[size_t(j) * a.V]), acc0);
-        acc1 = fmaf(s_e[j + 1], bf16_to_f32(w2[size_t(j + 1) * a.V]), acc1);
+      for (int j = j0; j < j1; ++j) {
+        const uint32_t pr = *reinterpret_cast<const uint32_t*>(w2 + size_t(j) * a.V);   // V even: 4-byte aligned
+        acc = fma2(make_float2(s_e[j], s_e[j]), make_float2(__uint_as_float(pr << 16), __uint_as_float(pr & 0xFFFF0000u)),
+                   acc);
       }
-      s_chunk[q][c] = acc0 + acc1;
     }
+    s_wsum[warp][2 * lane] = acc.x;
+    s_wsum[warp][2 * lane + 1] = acc.y;
     __syncthreads();
     if (threadIdx.x < 64) {
+      const int c = threadIdx.x, v = sel * 64 + c;
       float x = neg_inf();
       if (!bad && v < a.V) {
-        x = bf16_to_f32(a.U[(size_t(r) * a.gamma + (a.k - 1)) * a.V + v]) +
-            ((s_chunk[0][c] + s_chunk[1][c]) + (s_chunk[2][c] + s_chunk[3][c]));
+        float dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSampleWarps; ++w) dot += s_wsum[w][c];
+        x = bf16_to_f32(a.U[(size_t(r) * a.gamma + (a.k - 1)) * a.V + v]) + dot;
         if (a.logits_bf16) x = round_to_bf16(x);
       }
       s_chunk[0][c] = x;                       // the tile's logits, in column order
