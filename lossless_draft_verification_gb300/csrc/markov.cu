@@ -71,6 +71,13 @@ struct MarkovArgs {
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
+// two floats rounded to bf16 (round to nearest even) and packed, x in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ float round_to_bf16(float x) {
   // round-to-nearest-even to bf16, back to float (finite inputs)
   uint32_t u = __float_as_uint(x);
@@ -206,6 +213,10 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
   const MarkovPart* part = a.part + size_t(r) * a.ntile;
   const float u = a.greedy ? 0.f : a.uniforms[size_t(r) * a.gamma + (a.k - 1)];
   const bool bad_in = x_prev < 0 || x_prev >= a.V || (!a.greedy && !(u >= 0.f && u < 1.f));
+  // the conditioning row W1[x_{k-1}] of a tile recompute, fetched while the
+  // partials are combined (it does not depend on the selected tile)
+  if (a.logits == nullptr && !a.greedy && !bad_in)
+    for (int j = threadIdx.x; j < a.rank; j += kSampleThreads) s_e[j] = bf16_to_f32(a.W1[size_t(x_prev) * a.rank + j]);
   int tok = -1;
   if (a.greedy) {
     float v = neg_inf();
@@ -324,11 +335,7 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
     // 4-byte load per row, all independent; the warps' float32 sums are then
     // added in warp order.
-    if (!bad)
-      for (int j = threadIdx.x; j < a.rank; j += kSampleThreads)
-        s_e[j] = bf16_to_f32(a.W1[size_t(x_prev) * a.rank + j]);
-    __syncthreads();
-    const int v2 = sel * 64 + 2 * lane;                  // this lane's column pair
+    const int v2 = sel * 64 + 2 * lane;                  // this lane's column pair (s_e was filled at the start)
     const int per_w = (a.rank + kSampleWarps - 1) / kSampleWarps;
     float2 acc = make_float2(0.f, 0.f);
     if (!bad && v2 < a.V) {
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
 #pragma unroll
         for (int w = 0; w < kSampleWarps; ++w) dot += s_wsum[w][c];
         x = bf16_to_f32(a.U[(size_t(r) * a.gamma + (a.k - 1)) * a.V + v]) + dot;
-        if (a.logits_bf16) x = round_to_bf16(x);
+        if (a.logits_bf16) x = __uint_as_float(pack_bf16x2(x, 0.f) << 16);
       }
       s_chunk[0][c] = x;                       // the tile's logits, in column order
     }
@@ -907,8 +914,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
             float2 x = add2(ub, ac);
             if (a.logits_bf16) {                  // the draw uses the logits rounded to bf16
-              x.x = round_to_bf16(x.x);
-              x.y = round_to_bf16(x.y);
+              const uint32_t pk = pack_bf16x2(x.x, x.y);
+              x = make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xFFFF0000u));
             }
             L[j] = x.x;
             L[j + 1] = x.y;
@@ -1232,7 +1239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
             const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
             const float2 x = add2(ub, ac);
-            ow[e >> 1] = (__float_as_uint(round_to_bf16(x.x)) >> 16) | (__float_as_uint(round_to_bf16(x.y)) & 0xFFFF0000u);
+            ow[e >> 1] = pack_bf16x2(x.x, x.y);   // the rounding the draws used
           }
           o[cc] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
         }
