@@ -732,7 +732,7 @@ constexpr uint32_t kWIdesc = tc::idesc_bf16_f32(kTcBM, kWN, true);     // B = W2
 
 __global__ void __launch_bounds__(kWThreads, 1)
     markov_tcw_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
-                      MarkovTcArgs ta) {
+                      const __grid_constant__ CUtensorMap tmap_l, MarkovTcArgs ta) {
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
   __shared__ __align__(8) uint64_t bar_full[kWStagesB], bar_empty[kWStagesB], bar_ufull[2][kWStagesU],
@@ -921,9 +921,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
             L[j + 1] = x.y;
           }
         }
+        if (a.logits != nullptr) {
+          // bf16 logits kept: this warp's 32 rows of the chunk go out through its
+          // own 4 KB part of the U slot (its values are consumed), in the
+          // 128-byte swizzle the TMA store expects, one 64-column box.
+          uint8_t* wst = const_cast<uint8_t*>(urow) + size_t(qd) * 32 * kTcRowBytes;
+          __syncwarp();
+          const int z = row0 + qd * 32;
+          if (a.logits_bf16) {                   // (float32 logits are stored by markov_tc_kernel)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<uint4*>(wst + sw128(lane, cc)) =
+                  make_uint4((__float_as_uint(L[8 * cc + 0]) >> 16) | (__float_as_uint(L[8 * cc + 1]) & 0xFFFF0000u),
+                             (__float_as_uint(L[8 * cc + 2]) >> 16) | (__float_as_uint(L[8 * cc + 3]) & 0xFFFF0000u),
+                             (__float_as_uint(L[8 * cc + 4]) >> 16) | (__float_as_uint(L[8 * cc + 5]) & 0xFFFF0000u),
+                             (__float_as_uint(L[8 * cc + 6]) >> 16) | (__float_as_uint(L[8 * cc + 7]) & 0xFFFF0000u));
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tc::tma_store_3d(&tmap_l, n0, ta.lz, z, wst);
+              tc::bulk_commit();
+              tc::bulk_wait_read_all();
+            }
+          }
+        }
         // The slot is released only now: the adds above consumed every value
-        // read from it, so no read can still be outstanding when the copy of a
-        // later chunk overwrites it.
+        // read from it (and a store has read what was staged in it), so no read
+        // can still be outstanding when the copy of a later chunk overwrites it.
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_uempty[g][us]);
         if (n0 + 64 > a.V) {
@@ -964,6 +988,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       }
       if (!ok) break;
     }
+    if (lane == 0 && a.logits != nullptr) tc::bulk_wait_all();   // logits written before the sampler reads them
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1414,11 +1439,12 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SPECV_ERR_CUDA;
     }
-    // Logits kept: the 64-column kernel stages and stores them.  None kept: the
-    // 256-column kernel, which writes only the tile partials.
-    const bool store = draft_logits != nullptr;
-    void* tc_fn = store ? reinterpret_cast<void*>(&markov_tc_kernel<2>) : reinterpret_cast<void*>(&markov_tcw_kernel);
-    const size_t tc_bytes = store ? tc_smem(2, true) : kWSmem;
+    // 256-column tiles, with kept bf16 logits leaving through the U slots; kept
+    // float32 logits (twice the bytes per chunk) use the 64-column kernel, whose
+    // own staging lets both halves of a chunk's store go out without waiting
+    const bool wide = draft_logits == nullptr || a.logits_bf16;
+    void* tc_fn = wide ? reinterpret_cast<void*>(&markov_tcw_kernel) : reinterpret_cast<void*>(&markov_tc_kernel<2>);
+    const size_t tc_bytes = wide ? kWSmem : tc_smem(2, true);
     if (cudaFuncSetAttribute(tc_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tc_bytes)) != cudaSuccess)
       return SPECV_ERR_CUDA;
     MarkovTcArgs ta;
@@ -1447,11 +1473,10 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       cfg.attrs = at;
       cfg.numAttrs = 1;
       void* targs[] = {&tmap_w2, &tmap_u, &tmap_l, &ta};
-      void* wargs[] = {&tmap_w2, &tmap_u, &ta};
       cfg.gridDim = g1;
-      cfg.blockDim = dim3(store ? kTcThreads : kWThreads);
+      cfg.blockDim = dim3(wide ? kWThreads : kTcThreads);
       cfg.dynamicSmemBytes = tc_bytes;
-      if (cudaLaunchKernelExC(&cfg, tc_fn, store ? targs : wargs) != cudaSuccess)
+      if (cudaLaunchKernelExC(&cfg, tc_fn, targs) != cudaSuccess)
         return SPECV_ERR_CUDA;
       void* sargs[] = {&a};
       cfg.gridDim = dim3(unsigned(R));
