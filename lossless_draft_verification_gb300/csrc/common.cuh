@@ -158,6 +158,13 @@ __device__ __forceinline__ bool mbar_wait_parity(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// arrive on an mbarrier given by its shared::cluster address, in this CTA or
+// another CTA of the cluster.  The default CTA-scope release: a cluster-scope
+// one would also wait for this thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global memory into this CTA's shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -85,6 +85,79 @@ __device__ __forceinline__ float round_to_bf16(float x) {
   return __uint_as_float(u & 0xFFFF0000u);
 }
 
+// float(bf16 low half of w) + lo and float(bf16 high half) + hi, each one f32
+// add rounded to nearest (the conversions are exact)
+__device__ __forceinline__ float2 add_bf16x2(uint32_t w, float lo, float hi) {
+  float x, y;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, %3;\n add.rn.f32.bf16 %1, h, %4;\n}"
+      : "=f"(x), "=f"(y) : "r"(w), "f"(lo), "f"(hi));
+  return make_float2(x, y);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// One row's 64-column chunk of L = U + W1[x] . W2: u holds its 64 bf16 U
+// values as eight 16-byte granules, acc0 / acc1 its accumulator columns 0-31 /
+// 32-63; rounded to bf16 when that is the draw precision.
+__device__ __forceinline__ void chunk_logits(const uint4 (&u)[8], const float (&acc0)[32], const float (&acc1)[32],
+                                             bool to_bf16, float (&L)[64]) {
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    const uint32_t wv[4] = {u[cc].x, u[cc].y, u[cc].z, u[cc].w};
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const int j = 8 * cc + e;
+      float2 x = j < 32 ? add_bf16x2(wv[e >> 1], acc0[j], acc0[j + 1]) : add_bf16x2(wv[e >> 1], acc1[j - 32], acc1[j - 31]);
+      if (to_bf16) {
+        const uint32_t pk = pack_bf16x2(x.x, x.y);
+        x = make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xFFFF0000u));
+      }
+      L[j] = x.x;
+      L[j + 1] = x.y;
+    }
+  }
+}
+
+// The tile partial of one row's 64-column chunk whose columns past V hold -inf:
+// (max, argmax) at T = 0, else (max * c2, sum 2^(L * c2 - max * c2)).  Maxima
+// by three-input max in a depth-4 tree; the sum in four packed chains.
+__device__ __forceinline__ MarkovPart chunk_partial(const float (&L)[64], int n0, const MarkovArgs& a) {
+  MarkovPart p;
+  if (a.greedy) {
+    float m = L[0];
+    int idx = n0;
+#pragma unroll
+    for (int j = 1; j < 64; ++j)
+      if (L[j] > m) { m = L[j]; idx = n0 + j; }
+    p.a = m;
+    p.b = __int_as_float(idx);
+    return p;
+  }
+  float m1[22], m2[8];
+#pragma unroll
+  for (int j = 0; j < 21; ++j) m1[j] = max3(L[3 * j], L[3 * j + 1], L[3 * j + 2]);
+  m1[21] = L[63];
+#pragma unroll
+  for (int j = 0; j < 7; ++j) m2[j] = max3(m1[3 * j], m1[3 * j + 1], m1[3 * j + 2]);
+  m2[7] = m1[21];
+  const float mx = max3(max3(m2[0], m2[1], m2[2]), max3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+  const float m_c2 = mx * a.c2;
+  const float2 c2v = make_float2(a.c2, a.c2), mv = make_float2(-m_c2, -m_c2);
+  float2 z[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const float2 tt = fma2(make_float2(L[j], L[j + 1]), c2v, mv);
+    z[(j >> 1) & 3] = add2(z[(j >> 1) & 3], make_float2(ex2(tt.x), ex2(tt.y)));
+  }
+  p.a = m_c2;
+  p.b = ((z[0].x + z[0].y) + (z[1].x + z[1].y)) + ((z[2].x + z[2].y) + (z[3].x + z[3].y));
+  return p;
+}
+
 __device__ __forceinline__ int prev_token(const MarkovArgs& a, int r) {
   return a.k == 1 ? a.anchor[r] : a.tokens[size_t(r) * a.gamma + (a.k - 2)];
 }
@@ -198,7 +271,7 @@ constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kSampleMaxPer = 16;     // tiles per thread: at most 4096 tiles per row
 constexpr int kSampleMaxRank = 256;   // rank of the tensor-core form, whose tiles may be recomputed
 
-__global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArgs a) {
+__global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(MarkovArgs a) {
   __shared__ float s_e[kSampleMaxRank];  // W1[x_{k-1}] when the tile is recomputed
   __shared__ float s_wsum[kSampleWarps][64];   // per-warp rank sums of the recomputed tile
   __shared__ float s_chunk[1][64];       // the recomputed tile
@@ -206,6 +279,9 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
   __shared__ int s_i[kSampleWarps];
   __shared__ int s_sel;
   __shared__ float s_base, s_target;
+  // The next step's grid may be scheduled now (it sets up and then waits, in
+  // griddepcontrol.wait, for this grid to complete).
+  pdl_launch_dependents();
   pdl_wait_primary();                      // the logits and partials of this step are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x;
@@ -237,7 +313,6 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
         a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad_in ? -1 : i;
         if (bad_in) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
       }
-      pdl_launch_dependents();
     }
     return;
   }
@@ -335,6 +410,9 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
     // 4-byte load per row, all independent; the warps' float32 sums are then
     // added in warp order.
+    // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
+    // 4-byte load per row, all independent; the warps' float32 sums are then
+    // added in warp order.
     const int v2 = sel * 64 + 2 * lane;                  // this lane's column pair (s_e was filled at the start)
     const int per_w = (a.rank + kSampleWarps - 1) / kSampleWarps;
     float2 acc = make_float2(0.f, 0.f);
@@ -365,7 +443,7 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     }
     __syncthreads();
   }
-  if (warp != 0) return;                   // warp 0 triggers the next step once the token is written
+  if (warp != 0) return;                   // warp 0 rescans the selected tile and writes the token
   if (!bad) {
     // rescan the selected tile's columns in index order
     const MarkovPart p = part[sel];
@@ -409,7 +487,6 @@ __global__ void __launch_bounds__(kSampleThreads) markov_sample_kernel(MarkovArg
     a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad ? -1 : tok;
     if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
-  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -444,6 +521,24 @@ struct MarkovTcArgs {
 // 16-byte granule g of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int g) { return uint32_t(r) * kTcRowBytes + (uint32_t(g ^ (r & 7)) << 4); }
 
+// The A operand E[r, :] = W1[x(r), :] of a 128-row block in the canonical
+// K-major 128-byte-swizzle layout (nkc chunks of [128 rows][128 B]), written by
+// the 256 threads tid < 256: thread tid takes row tid % 128 and half tid / 128
+// of its 16-byte granules, all issued as asynchronous copies before one wait
+// (x < 0: a zero row).  The caller fences for the tensor core afterwards.
+static_assert(kTcEpiWarps * 32 == 2 * kTcBM, "gather_w1_rows: two threads per row");
+__device__ __forceinline__ void gather_w1_rows(uint8_t* sE, const uint16_t* W1, int rank, int nkc, int tid, int x) {
+  const int r = tid & (kTcBM - 1), h = tid / kTcBM;
+  const int half = nkc * 4;                       // granules per thread: half of the row's rank / 8
+  for (int gi = h * half; gi < (h + 1) * half; ++gi) {
+    uint8_t* dst = sE + size_t(gi >> 3) * (kTcBM * kTcRowBytes) + sw128(r, gi & 7);
+    if (x >= 0) cp_async16(dst, W1 + size_t(x) * rank + gi * 8);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
+}
+
 template <int NS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     markov_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
@@ -463,7 +558,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb = blockIdx.x / ta.per_mb, j0 = blockIdx.x - (blockIdx.x / ta.per_mb) * ta.per_mb;
   const int row0 = mb * kTcBM;
-  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -481,23 +575,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
+  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
+  // for this grid to complete.
+  pdl_launch_dependents();
   pdl_wait_primary();                      // the previous step's tokens are complete
+  // the error word is reset once per call, after the work before it completes
+  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
   if (warp < kTcEpiWarps) {
-    // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
-    for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
-      const int req = row0 + r;
+    // A operand: E[r, :] = W1[x_{k-1}(r), :] for this CTA's 128 rows
+    {
+      const int req = row0 + (threadIdx.x & (kTcBM - 1));
       int x = -1;
       if (req < a.R) {
         x = prev_token(a, req);
         if (x < 0 || x >= a.V) x = -1;
       }
-      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
-      for (int kc = 0; kc < ta.nkc; ++kc) {
-        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(dst + sw128(r, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
-      }
+      gather_w1_rows(sE, a.W1, a.rank, ta.nkc, threadIdx.x, x);
     }
     tc::fence_proxy_async_smem();
   }
@@ -598,25 +691,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tempty[g]);
-      // L = U + acc, two columns per packed add
       float L[64];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t wv[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int j = 8 * c + e;
-          const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
-          const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
-          float2 x = add2(ub, ac);
-          if (a.logits_bf16) {
-            x.x = round_to_bf16(x.x);
-            x.y = round_to_bf16(x.y);
-          }
-          L[j] = x.x;
-          L[j + 1] = x.y;
-        }
-      }
+      chunk_logits(u, acc0, acc1, a.logits_bf16 != 0, L);
       // release the U stage only after the adds above consumed its values
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_uempty[us]);
@@ -659,36 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (!rv) continue;
-      MarkovPart mpart;
-      if (a.greedy) {
-        float m = L[0];
-        int idx = n0;
-#pragma unroll
-        for (int j = 1; j < 64; ++j)
-          if (L[j] > m) { m = L[j]; idx = n0 + j; }
-        mpart.a = m;
-        mpart.b = __int_as_float(idx);
-      } else {
-        // tree maximum (short dependency chains), then four packed partial sums
-        float mx[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(L[j], L[j + 16]), fmaxf(L[j + 32], L[j + 48]));
-#pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-        const float m_c2 = mx[0] * a.c2;
-        const float2 c2v = make_float2(a.c2, a.c2), mv = make_float2(-m_c2, -m_c2);
-        float2 z[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float2 tt = fma2(make_float2(L[j], L[j + 1]), c2v, mv);
-          z[(j >> 1) & 3] = add2(z[(j >> 1) & 3], make_float2(ex2(tt.x), ex2(tt.y)));
-        }
-        mpart.a = m_c2;
-        mpart.b = ((z[0].x + z[0].y) + (z[1].x + z[1].y)) + ((z[2].x + z[2].y) + (z[3].x + z[3].y));
-      }
-      a.part[size_t(r) * a.ntile + t] = mpart;
+      a.part[size_t(r) * a.ntile + t] = chunk_partial(L, n0, a);
     }
     if (NS == 2 && lane == 0 && a.logits != nullptr) tc::bulk_wait_all();   // logits written before the sampler reads them
   }
@@ -699,7 +746,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tmem_dealloc(tmem, kTcTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
-  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -748,7 +794,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int mb = blockIdx.x / ta.per_mb, j0 = blockIdx.x - (blockIdx.x / ta.per_mb) * ta.per_mb;
   const int row0 = mb * kTcBM;
   const int nwt = (ta.ntiles + kWChunks - 1) / kWChunks;       // 256-column tiles
-  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStagesB; ++i) {
@@ -769,23 +814,22 @@ __global__ void __launch_bounds__(kWThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 3) tc::tmem_alloc(&s_tmem, kWTmemCols);
+  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
+  // for this grid to complete.
+  pdl_launch_dependents();
   pdl_wait_primary();                      // the previous step's tokens are complete
+  // the error word is reset once per call, after the work before it completes
+  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
   if (warp < kTcEpiWarps) {
-    // A operand: E[r, :] = W1[x_{k-1}(r), :], canonical K-major 128-byte-swizzle layout
-    for (int r = threadIdx.x; r < kTcBM; r += kTcEpiWarps * 32) {
-      const int req = row0 + r;
+    // A operand: E[r, :] = W1[x_{k-1}(r), :] for this CTA's 128 rows
+    {
+      const int req = row0 + (threadIdx.x & (kTcBM - 1));
       int x = -1;
       if (req < a.R) {
         x = prev_token(a, req);
         if (x < 0 || x >= a.V) x = -1;
       }
-      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
-      for (int kc = 0; kc < ta.nkc; ++kc) {
-        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(dst + sw128(r, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
-      }
+      gather_w1_rows(sE, a.W1, a.rank, ta.nkc, threadIdx.x, x);
     }
     tc::fence_proxy_async_smem();
   }
@@ -904,23 +948,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4*>(urow + sw128(rl, cc));
         const int n0 = t * kWN + c * 64;
         float L[64];
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t wv[4] = {u[cc].x, u[cc].y, u[cc].z, u[cc].w};
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int j = 8 * cc + e;
-            const float2 ub = make_float2(__uint_as_float(wv[e >> 1] << 16), __uint_as_float(wv[e >> 1] & 0xFFFF0000u));
-            const float2 ac = j < 32 ? make_float2(acc0[j], acc0[j + 1]) : make_float2(acc1[j - 32], acc1[j - 31]);
-            float2 x = add2(ub, ac);
-            if (a.logits_bf16) {                  // the draw uses the logits rounded to bf16
-              const uint32_t pk = pack_bf16x2(x.x, x.y);
-              x = make_float2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xFFFF0000u));
-            }
-            L[j] = x.x;
-            L[j + 1] = x.y;
-          }
-        }
+        chunk_logits(u, acc0, acc1, a.logits_bf16, L);
         if (a.logits != nullptr) {
           // bf16 logits kept: this warp's 32 rows of the chunk go out through its
           // own 4 KB part of the U slot (its values are consumed), in the
@@ -956,35 +984,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             if (n0 + j >= a.V) L[j] = neg_inf();
         }
         if (!rv || n0 >= a.V) continue;
-        MarkovPart mpart;
-        if (a.greedy) {
-          float m = L[0];
-          int idx = n0;
-#pragma unroll
-          for (int j = 1; j < 64; ++j)
-            if (L[j] > m) { m = L[j]; idx = n0 + j; }
-          mpart.a = m;
-          mpart.b = __int_as_float(idx);
-        } else {
-          float mx[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(L[j], L[j + 16]), fmaxf(L[j + 32], L[j + 48]));
-#pragma unroll
-          for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-          const float m_c2 = mx[0] * a.c2;
-          const float2 c2v = make_float2(a.c2, a.c2), mv = make_float2(-m_c2, -m_c2);
-          float2 z[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float2 tt = fma2(make_float2(L[j], L[j + 1]), c2v, mv);
-            z[(j >> 1) & 3] = add2(z[(j >> 1) & 3], make_float2(ex2(tt.x), ex2(tt.y)));
-          }
-          mpart.a = m_c2;
-          mpart.b = ((z[0].x + z[0].y) + (z[1].x + z[1].y)) + ((z[2].x + z[2].y) + (z[3].x + z[3].y));
-        }
-        a.part[size_t(r) * a.ntile + (n0 >> 6)] = mpart;
+        a.part[size_t(r) * a.ntile + (n0 >> 6)] = chunk_partial(L, n0, a);
       }
       if (!ok) break;
     }
@@ -997,7 +997,238 @@ __global__ void __launch_bounds__(kWThreads, 1)
     tc::tmem_dealloc(tmem, kWTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// markov_tc2: the same step on CTA pairs.  A cluster of two CTAs (two SMs)
+// owns two 128-request blocks, one per CTA, and a strided set of 256-column
+// tiles.  One thread of the even CTA issues tcgen05.mma.cta_group::2 with
+// M = 256 (each CTA contributes the W1 rows of its own block), N = 256 and
+// K = 16, so each CTA stages only its half of every W2 tile (128 columns):
+// half the W2 bytes per SM of markov_tcw and twice the ring stages in the same
+// shared memory.  Each CTA's tensor memory holds its own 128 accumulator rows;
+// its epilogue is markov_tcw's without logit stores: this is the form for
+// drafting that keeps no logits (with kept logits the step is bound by their
+// DRAM writes and markov_tcw / markov_tc are as fast).
+//
+// Cross-CTA protocol: each CTA's W2 copies complete on the even CTA's full
+// barrier (which expects both halves); the MMA commits arrive on the empty and
+// accumulator-full barriers of both CTAs; both CTAs' epilogue warps arrive on
+// the even CTA's accumulator-empty barrier.  Every wait is bounded, each CTA
+// waits until the last commits aimed at it have arrived, and a cluster barrier
+// precedes exit, so no copy or arrival targets a CTA that has exited.
+constexpr int kPN = kWN / 2;                                        // W2 columns per CTA per tile
+constexpr size_t kPStageB = size_t(kPN / 64) * 64 * kTcRowBytes;     // 16 KB: 64 rank rows x 128 columns
+constexpr int kPStagesB = 6;                                        // W2 ring
+constexpr size_t kPSmem = kTcSmemE + kPStagesB * kPStageB + 2 * kWStagesU * kWStageU + 1024;
+constexpr uint32_t kPIdesc = tc::idesc_bf16_f32(2 * kTcBM, kWN, true);   // M = 256 over the pair, B MN-major
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    markov_tc2_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
+                      MarkovTcArgs ta) {
+  constexpr int NS = kPStagesB;
+  const MarkovArgs& a = ta.m;
+  extern __shared__ uint8_t s_raw[];
+  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_ufull[2][kWStagesU], bar_uempty[2][kWStagesU],
+      bar_tfull[2], bar_tempty[2], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_err;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
+  uint8_t* sB = sE + kTcSmemE;                      // [stage][column block][64 k-rows][128 B]
+  uint8_t* sU = sB + NS * kPStageB;                 // [group][stage][128 rows][128 B]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = int(cluster_ctarank());         // 0: issues the pair MMAs
+  const int cl = int(blockIdx.x >> 1);
+  const int pb = cl / ta.per_mb, j0 = cl - pb * ta.per_mb;
+  const int row0 = (2 * pb + crank) * kTcBM;
+  const int nwt = (ta.ntiles + kWChunks - 1) / kWChunks;       // 256-column tiles
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1);
+    }
+    for (int g = 0; g < 2; ++g)
+      for (int i = 0; i < kWStagesU; ++i) {
+        mbar_init(&bar_ufull[g][i], 1);
+        mbar_init(&bar_uempty[g][i], 4);
+      }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_tfull[i], 1);
+      mbar_init(&bar_tempty[i], 2 * 4);          // four epilogue warps of each CTA
+    }
+    mbar_init(&bar_done, 1);
+    s_err = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTcEpiWarps + 3) tc::tmem_alloc_pair(&s_tmem, kWTmemCols);
+  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
+  // for this grid to complete.
   pdl_launch_dependents();
+  pdl_wait_primary();                      // the previous step's tokens are complete
+  // the error word is reset once per call, after the work before it completes
+  if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
+  if (warp < kTcEpiWarps) {
+    // A operand: E[r, :] = W1[x_{k-1}(r), :] for this CTA's 128 rows
+    {
+      const int req = row0 + (threadIdx.x & (kTcBM - 1));
+      int x = -1;
+      if (req < a.R) {
+        x = prev_token(a, req);
+        if (x < 0 || x >= a.V) x = -1;
+      }
+      gather_w1_rows(sE, a.W1, a.rank, ta.nkc, threadIdx.x, x);
+    }
+    tc::fence_proxy_async_smem();
+  }
+  // Both CTAs' barriers are initialised and both A halves written before any
+  // copy, arrival or MMA crosses to the other CTA.
+  tc::fence_before_sync();
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kTcEpiWarps) {
+    // ---- W2 producer: this CTA's 128 columns of one (tile, rank chunk) per stage
+    if (lane == 0) {
+      const uint64_t keep = tc::policy_evict_last();
+      int q = 0;                                   // (tile, chunk) sequence number
+      for (int t = j0; t < nwt; t += ta.per_mb)
+        for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
+          const int s = q % NS;
+          if (!mbar_wait_parity(&bar_empty[s], ((q / NS) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
+          if (crank == 0) mbar_arrive_expect_tx(&bar_full[s], uint32_t(2 * kPStageB));
+          const uint32_t full0 = cluster_map_shared(&bar_full[s], 0);
+          for (int b = 0; b < kPN / 64; ++b)
+            tc::tma_load_2d_pair(sB + size_t(s) * kPStageB + size_t(b) * (64 * kTcRowBytes), &tmap_w2,
+                                 t * kWN + crank * kPN + b * 64, kc * 64, full0, keep);
+        }
+      // the MMAs that read the last stages have completed, and their commits
+      // to this CTA have arrived
+      for (int d = (q >= NS ? q - NS : 0); d < q; ++d)
+        if (!mbar_wait_parity(&bar_empty[d % NS], (d / NS) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 1 || warp == kTcEpiWarps + 2) {
+    // ---- U producer of epilogue group g: 64-column chunks of this CTA's U_k rows
+    const int g = warp - (kTcEpiWarps + 1);
+    if (lane == 0) {
+      const uint64_t once = tc::policy_evict_first();
+      uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+      int q = 0;
+      for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb)
+        for (int c = 0; c < kWChunks; ++c, ++q) {
+          const int s = q % kWStagesU;
+          if (!mbar_wait_parity(&bar_uempty[g][s], ((q / kWStagesU) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
+          mbar_arrive_expect_tx(&bar_ufull[g][s], uint32_t(kWStageU));
+          tc::tma_load_3d_hint(ring + size_t(s) * kWStageU, &tmap_u, t * kWN + c * 64, a.k - 1, row0,
+                               &bar_ufull[g][s], once);
+        }
+      for (int d = (q >= kWStagesU ? q - kWStagesU : 0); d < q; ++d)
+        if (!mbar_wait_parity(&bar_ufull[g][d % kWStagesU], (d / kWStagesU) & 1, kTcMaxPolls)) s_err = 1;
+    }
+  } else if (warp == kTcEpiWarps + 3) {
+    // ---- pair MMA issuer (even CTA)
+    if (lane == 0 && crank == 0) {
+      const uint64_t da0 = tc::smem_desc_k_sw128(smem_addr(sE));
+      const uint64_t db0 = tc::smem_desc_mn_sw128(smem_addr(sB), 1024, 64 * kTcRowBytes);
+      int q = 0, i = 0;
+      bool ok = true;
+      for (int t = j0; t < nwt && ok; t += ta.per_mb, ++i) {
+        const int tb = i & 1;
+        if (!mbar_wait_parity(&bar_tempty[tb], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t dtm = tmem + uint32_t(tb * kWN);
+        for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
+          const int s = q % NS;
+          if (!mbar_wait_parity(&bar_full[s], (q / NS) & 1, kTcMaxPolls)) { s_err = 1; ok = false; break; }
+          tc::fence_after_sync();
+          const uint64_t dbs = db0 + uint64_t(s) * (kPStageB / 16);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: chunk kc (16 KB apart), 32-byte K step; B: 16 k-rows = two 1024-byte groups
+            const uint64_t da = da0 + uint64_t(kc * (kTcBM * kTcRowBytes / 16) + kk * 2);
+            const uint64_t db = dbs + uint64_t(kk * (2048 / 16));
+            tc::mma_bf16_pair(dtm, da, db, kPIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit_pair(&bar_empty[s], 0x3);    // both CTAs' stage s is free once these MMAs have read it
+        }
+        if (ok) tc::commit_pair(&bar_tfull[tb], 0x3);   // both accumulator halves are ready
+      }
+      tc::commit_pair(&bar_done, 0x1);
+      if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
+      // both CTAs' epilogues have released the accumulators of the last tiles
+      for (int tb = 0; tb < 2; ++tb) {
+        const int uses = (i + 1 - tb) / 2;
+        if (uses > 0 && !mbar_wait_parity(&bar_tempty[tb], (uses - 1) & 1, kTcMaxPolls)) s_err = 1;
+      }
+    }
+  } else {
+    // ---- epilogue group g = warp / 4 takes tiles i = g, g + 2, ...; thread = request row
+    const int g = warp >> 2, qd = warp & 3;
+    const int rl = qd * 32 + lane;
+    const int r = row0 + rl;
+    const bool rv = r < a.R;
+    const uint32_t tempty0 = cluster_map_shared(&bar_tempty[g], 0);
+    uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+    int i = g;
+    for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb, i += 2) {
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], (i >> 1) & 1, kTcMaxPolls))) {
+        s_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      bool ok = true;
+      for (int c = 0; c < kWChunks; ++c) {
+        const int q = (i >> 1) * kWChunks + c, us = q % kWStagesU;   // this group's chunk sequence
+        float acc0[32], acc1[32];
+        const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(g * kWN + c * 64);
+        tc::tmem_ld32(taddr, acc0);
+        tc::tmem_ld32(taddr + 32, acc1);
+        tc::tmem_ld_wait();
+        if (c == kWChunks - 1) {               // this CTA's half of the accumulator has been read
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_ufull[g][us], (q / kWStagesU) & 1, kTcMaxPolls))) {
+          s_err = 1;
+          ok = false;
+          break;
+        }
+        uint4 u[8];
+        const uint8_t* urow = ring + size_t(us) * kWStageU;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4*>(urow + sw128(rl, cc));
+        const int n0 = t * kWN + c * 64;
+        float L[64];
+        chunk_logits(u, acc0, acc1, a.logits_bf16, L);
+        // The U slot is released once the adds above have consumed every value
+        // read from it, so no read is outstanding when a later copy refills it.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_uempty[g][us]);
+        if (n0 + 64 > a.V) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (n0 + j >= a.V) L[j] = neg_inf();
+        }
+        if (rv && n0 < a.V) a.part[size_t(r) * a.ntile + (n0 >> 6)] = chunk_partial(L, n0, a);
+      }
+      if (!ok) break;
+    }
+  }
+  tc::fence_before_sync();
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (warp == kTcEpiWarps + 3) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, kWTmemCols);
+  }
+  if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
@@ -1108,7 +1339,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kWTmemCols);
   if (warp < kTcEpiWarps) {
     // A operand: the previous token of each listed row
-    for (int rl = threadIdx.x; rl < kTcBM; rl += kTcEpiWarps * 32) {
+    {
+      const int rl = threadIdx.x & (kTcBM - 1);
       int x = -1;
       if (row0 + rl < n_rows) {
         const int rk = a.rows[row0 + rl];
@@ -1116,13 +1348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         x = k == 0 ? a.anchor[r] : a.tokens[size_t(r) * a.gamma + (k - 1)];
         if (x < 0 || x >= a.V) x = -1;
       }
-      const uint4* src = x >= 0 ? reinterpret_cast<const uint4*>(a.W1 + size_t(x) * a.rank) : nullptr;
-      for (int kc = 0; kc < a.nkc; ++kc) {
-        uint8_t* dst = sE + size_t(kc) * (kTcBM * kTcRowBytes);
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<uint4*>(dst + sw128(rl, g)) = src ? __ldg(src + kc * 8 + g) : make_uint4(0u, 0u, 0u, 0u);
-      }
+      gather_w1_rows(sE, a.W1, a.rank, a.nkc, threadIdx.x, x);
     }
     tc::fence_proxy_async_smem();
   }
@@ -1349,6 +1575,35 @@ int sm_count() {
   }
   return n;
 }
+
+// Clusters of two CTAs of `fn` (one CTA per SM) that can be resident at once;
+// 0 on failure.  Cached per device.
+int pair_clusters(const void* fn, size_t smem_bytes) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kWThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 }  // namespace
 
 }  // namespace specv
@@ -1439,12 +1694,23 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SPECV_ERR_CUDA;
     }
-    // 256-column tiles, with kept bf16 logits leaving through the U slots; kept
-    // float32 logits (twice the bytes per chunk) use the 64-column kernel, whose
-    // own staging lets both halves of a chunk's store go out without waiting
+    // No logits kept and two or more 128-request blocks: CTA pairs (markov_tc2),
+    // two blocks per pair.  Otherwise single CTAs: 256-column tiles
+    // (markov_tcw), kept bf16 logits leaving through the U slots; kept float32
+    // logits (twice the bytes per chunk) use the 64-column kernel, whose own
+    // staging lets both halves of a chunk's store go out without waiting.
+    const int n_mb = (R + kTcBM - 1) / kTcBM;
+    const bool pair = n_mb >= 2 && draft_logits == nullptr;
     const bool wide = draft_logits == nullptr || a.logits_bf16;
-    void* tc_fn = wide ? reinterpret_cast<void*>(&markov_tcw_kernel) : reinterpret_cast<void*>(&markov_tc_kernel<2>);
-    const size_t tc_bytes = wide ? kWSmem : tc_smem(2, true);
+    void* tc_fn;
+    size_t tc_bytes;
+    if (pair) {
+      tc_fn = reinterpret_cast<void*>(&markov_tc2_kernel);
+      tc_bytes = kPSmem;
+    } else {
+      tc_fn = wide ? reinterpret_cast<void*>(&markov_tcw_kernel) : reinterpret_cast<void*>(&markov_tc_kernel<2>);
+      tc_bytes = wide ? kWSmem : tc_smem(2, true);
+    }
     if (cudaFuncSetAttribute(tc_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tc_bytes)) != cudaSuccess)
       return SPECV_ERR_CUDA;
     MarkovTcArgs ta;
@@ -1455,9 +1721,17 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     a.ntile = (V + kTcBN - 1) / kTcBN;
     ta.nkc = rank / 64;
     ta.ntiles = a.ntile;
-    const int n_mb = (R + kTcBM - 1) / kTcBM;
-    ta.per_mb = nsm / n_mb > 0 ? nsm / n_mb : 1;
-    const dim3 g1(unsigned(n_mb * ta.per_mb));
+    dim3 g1;
+    if (pair) {
+      const int n_pb = (n_mb + 1) / 2;
+      const int ncl = pair_clusters(tc_fn, tc_bytes);
+      if (ncl < 1) return SPECV_ERR_CUDA;
+      ta.per_mb = ncl / n_pb > 0 ? ncl / n_pb : 1;     // clusters per pair of request blocks
+      g1 = dim3(unsigned(2 * n_pb * ta.per_mb));
+    } else {
+      ta.per_mb = nsm / n_mb > 0 ? nsm / n_mb : 1;     // CTAs per request block
+      g1 = dim3(unsigned(n_mb * ta.per_mb));
+    }
     for (int k = 1; k <= gamma; ++k) {
       a.k = k;
       a.step_off = draft_logits ? long(k - 1) * V : 0;
@@ -1465,19 +1739,25 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
       ta.lz = draft_logits ? k - 1 : 0;
       // programmatic dependent launch: each grid is scheduled while its
       // predecessor drains and waits (griddepcontrol.wait) for its results
-      cudaLaunchAttribute at[1];
+      cudaLaunchAttribute at[2];
       at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       at[0].val.programmaticStreamSerializationAllowed = 1;
+      at[1].id = cudaLaunchAttributeClusterDimension;
+      at[1].val.clusterDim.x = 2;
+      at[1].val.clusterDim.y = 1;
+      at[1].val.clusterDim.z = 1;
       cudaLaunchConfig_t cfg = {};
       cfg.stream = st;
       cfg.attrs = at;
-      cfg.numAttrs = 1;
+      cfg.numAttrs = pair ? 2 : 1;
       void* targs[] = {&tmap_w2, &tmap_u, &tmap_l, &ta};
+      void* pargs[] = {&tmap_w2, &tmap_u, &ta};
       cfg.gridDim = g1;
-      cfg.blockDim = dim3(wide ? kWThreads : kTcThreads);
+      cfg.blockDim = dim3(pair || wide ? kWThreads : kTcThreads);
       cfg.dynamicSmemBytes = tc_bytes;
-      if (cudaLaunchKernelExC(&cfg, tc_fn, targs) != cudaSuccess)
+      if (cudaLaunchKernelExC(&cfg, tc_fn, pair ? pargs : targs) != cudaSuccess)
         return SPECV_ERR_CUDA;
+      cfg.numAttrs = 1;
       void* sargs[] = {&a};
       cfg.gridDim = dim3(unsigned(R));
       cfg.blockDim = dim3(kSampleThreads);
