@@ -158,6 +158,14 @@ __device__ __forceinline__ MarkovPart chunk_partial(const float (&L)[64], int n0
   return p;
 }
 
+// A tile partial, stored with an L2 eviction policy: evict_last keeps the
+// partials (R * ceil(V / 64) * 8 bytes) resident through the step's streamed
+// U and logit traffic until the sampler reads them.
+__device__ __forceinline__ void store_part(MarkovPart* dst, MarkovPart v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(v.a), "f"(v.b), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ int prev_token(const MarkovArgs& a, int r) {
   return a.k == 1 ? a.anchor[r] : a.tokens[size_t(r) * a.gamma + (a.k - 2)];
 }
@@ -279,14 +287,26 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
   __shared__ int s_i[kSampleWarps];
   __shared__ int s_sel;
   __shared__ float s_base, s_target;
+  __shared__ MarkovPart s_part[kSampleMaxPer * kSampleThreads * 9 / 8];   // tile t at t + t / 8
   // The next step's grid may be scheduled now (it sets up and then waits, in
   // griddepcontrol.wait, for this grid to complete).
   pdl_launch_dependents();
   pdl_wait_primary();                      // the logits and partials of this step are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x;
-  const int x_prev = prev_token(a, r);
   const MarkovPart* part = a.part + size_t(r) * a.ntile;
+  // T > 0: the row's tile partials go through shared memory, loaded first (they
+  // do not wait on the previous token) and coalesced: thread i takes tiles
+  // i, i + 256, ...; each thread later reads back its contiguous run, which the
+  // one 8-byte pad per 8 tiles keeps free of bank conflicts.
+  if (!a.greedy) {
+#pragma unroll
+    for (int j = 0; j < kSampleMaxPer; ++j) {
+      const int t = j * kSampleThreads + threadIdx.x;
+      if (t < a.ntile) s_part[t + (t >> 3)] = part[t];
+    }
+  }
+  const int x_prev = prev_token(a, r);
   const float u = a.greedy ? 0.f : a.uniforms[size_t(r) * a.gamma + (a.k - 1)];
   const bool bad_in = x_prev < 0 || x_prev >= a.V || (!a.greedy && !(u >= 0.f && u < 1.f));
   // the conditioning row W1[x_{k-1}] of a tile recompute, fetched while the
@@ -318,6 +338,7 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
   }
   // this thread's contiguous run of tiles, cached in registers; row maximum of
   // the tile maxima (already times c2)
+  __syncthreads();
   const int per = (a.ntile + kSampleThreads - 1) / kSampleThreads;     // <= kSampleMaxPer
   const int t0 = threadIdx.x * per, t1 = min(a.ntile, t0 + per);
   float pa[kSampleMaxPer], pb[kSampleMaxPer];
@@ -327,7 +348,8 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
     pa[j] = neg_inf();
     pb[j] = 0.f;
     if (t0 + j < t1) {
-      const MarkovPart p = part[t0 + j];
+      const int t = t0 + j;
+      const MarkovPart p = s_part[t + (t >> 3)];
       pa[j] = p.a;
       pb[j] = p.b;
       M = fmaxf(M, p.a);
@@ -667,6 +689,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rl = qd * 32 + lane;                  // row inside the 128-request block
     const int r = row0 + rl;
     const bool rv = r < a.R;
+    const uint64_t keep_part = tc::policy_evict_last();
     uint8_t* stage = sL + size_t(warp) * (2 * 32 * kTcRowBytes);
     int i = g;
     for (int t = j0 + g * ta.per_mb; t < ta.ntiles; t += 2 * ta.per_mb, i += 2) {
@@ -735,7 +758,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (!rv) continue;
-      a.part[size_t(r) * a.ntile + t] = chunk_partial(L, n0, a);
+      store_part(a.part + size_t(r) * a.ntile + t, chunk_partial(L, n0, a), keep_part);
     }
     if (NS == 2 && lane == 0 && a.logits != nullptr) tc::bulk_wait_all();   // logits written before the sampler reads them
   }
@@ -916,6 +939,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int rl = qd * 32 + lane;
     const int r = row0 + rl;
     const bool rv = r < a.R;
+    const uint64_t keep_part = tc::policy_evict_last();
     uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
     int i = g;
     for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb, i += 2) {
@@ -984,7 +1008,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             if (n0 + j >= a.V) L[j] = neg_inf();
         }
         if (!rv || n0 >= a.V) continue;
-        a.part[size_t(r) * a.ntile + (n0 >> 6)] = chunk_partial(L, n0, a);
+        store_part(a.part + size_t(r) * a.ntile + (n0 >> 6), chunk_partial(L, n0, a), keep_part);
       }
       if (!ok) break;
     }
@@ -1172,6 +1196,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int rl = qd * 32 + lane;
     const int r = row0 + rl;
     const bool rv = r < a.R;
+    const uint64_t keep_part = tc::policy_evict_last();
     const uint32_t tempty0 = cluster_map_shared(&bar_tempty[g], 0);
     uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
     int i = g;
@@ -1215,7 +1240,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           for (int j = 0; j < 64; ++j)
             if (n0 + j >= a.V) L[j] = neg_inf();
         }
-        if (rv && n0 < a.V) a.part[size_t(r) * a.ntile + (n0 >> 6)] = chunk_partial(L, n0, a);
+        if (rv && n0 < a.V) store_part(a.part + size_t(r) * a.ntile + (n0 >> 6), chunk_partial(L, n0, a), keep_part);
       }
       if (!ok) break;
     }
