@@ -1041,33 +1041,43 @@ __global__ void __launch_bounds__(kWThreads, 1)
 // the even CTA's accumulator-empty barrier.  Every wait is bounded, each CTA
 // waits until the last commits aimed at it have arrived, and a cluster barrier
 // precedes exit, so no copy or arrival targets a CTA that has exited.
-constexpr int kPN = kWN / 2;                                        // W2 columns per CTA per tile
-constexpr size_t kPStageB = size_t(kPN / 64) * 64 * kTcRowBytes;     // 16 KB: 64 rank rows x 128 columns
-constexpr int kPStagesB = 6;                                        // W2 ring
-constexpr size_t kPSmem = kTcSmemE + kPStagesB * kPStageB + 2 * kWStagesU * kWStageU + 1024;
-constexpr uint32_t kPIdesc = tc::idesc_bf16_f32(2 * kTcBM, kWN, true);   // M = 256 over the pair, B MN-major
+// TN: columns per tile (the MMA's N).  The tensor memory's 512 columns hold
+// 512 / TN accumulators; each CTA stages TN / 2 W2 columns per rank chunk in a
+// ring of 96 KB.
+template <int TN>
+struct PairShape {
+  static constexpr int kChunks = TN / 64;                               // 64-column chunks per tile
+  static constexpr int kAcc = 512 / TN;                                 // accumulators
+  static constexpr int kPN = TN / 2;                                    // W2 columns per CTA per tile
+  static constexpr size_t kStageB = size_t(kPN / 64) * 64 * kTcRowBytes;   // one rank chunk of them
+  static constexpr int kStages = int(96 * 1024 / kStageB);
+  static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(2 * kTcBM, TN, true);   // M = 256 over the pair, B MN-major
+};
+constexpr size_t kPSmem = kTcSmemE + 96 * 1024 + 2 * kWStagesU * kWStageU + 1024;
 
+template <int TN>
 __global__ void __launch_bounds__(kWThreads, 1)
     markov_tc2_kernel(const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_u,
                       MarkovTcArgs ta) {
-  constexpr int NS = kPStagesB;
+  using PS = PairShape<TN>;
+  constexpr int NS = PS::kStages, NACC = PS::kAcc, NCH = PS::kChunks;
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
   __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_ufull[2][kWStagesU], bar_uempty[2][kWStagesU],
-      bar_tfull[2], bar_tempty[2], bar_done;
+      bar_tfull[NACC], bar_tempty[NACC], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_err;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sE = smem;                               // [rank chunk][128 rows][128 B]
   uint8_t* sB = sE + kTcSmemE;                      // [stage][column block][64 k-rows][128 B]
-  uint8_t* sU = sB + NS * kPStageB;                 // [group][stage][128 rows][128 B]
+  uint8_t* sU = sB + NS * PS::kStageB;              // [group][stage][128 rows][128 B]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = int(cluster_ctarank());         // 0: issues the pair MMAs
   const int cl = int(blockIdx.x >> 1);
   const int pb = cl / ta.per_mb, j0 = cl - pb * ta.per_mb;
   const int row0 = (2 * pb + crank) * kTcBM;
-  const int nwt = (ta.ntiles + kWChunks - 1) / kWChunks;       // 256-column tiles
+  const int nwt = (ta.ntiles + NCH - 1) / NCH;                 // TN-column tiles
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -1079,7 +1089,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         mbar_init(&bar_ufull[g][i], 1);
         mbar_init(&bar_uempty[g][i], 4);
       }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NACC; ++i) {
       mbar_init(&bar_tfull[i], 1);
       mbar_init(&bar_tempty[i], 2 * 4);          // four epilogue warps of each CTA
     }
@@ -1117,7 +1127,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == kTcEpiWarps) {
-    // ---- W2 producer: this CTA's 128 columns of one (tile, rank chunk) per stage
+    // ---- W2 producer: this CTA's TN / 2 columns of one (tile, rank chunk) per stage
     if (lane == 0) {
       const uint64_t keep = tc::policy_evict_last();
       int q = 0;                                   // (tile, chunk) sequence number
@@ -1125,11 +1135,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
         for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
           const int s = q % NS;
           if (!mbar_wait_parity(&bar_empty[s], ((q / NS) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
-          if (crank == 0) mbar_arrive_expect_tx(&bar_full[s], uint32_t(2 * kPStageB));
+          if (crank == 0) mbar_arrive_expect_tx(&bar_full[s], uint32_t(2 * PS::kStageB));
           const uint32_t full0 = cluster_map_shared(&bar_full[s], 0);
-          for (int b = 0; b < kPN / 64; ++b)
-            tc::tma_load_2d_pair(sB + size_t(s) * kPStageB + size_t(b) * (64 * kTcRowBytes), &tmap_w2,
-                                 t * kWN + crank * kPN + b * 64, kc * 64, full0, keep);
+          for (int b = 0; b < PS::kPN / 64; ++b)
+            tc::tma_load_2d_pair(sB + size_t(s) * PS::kStageB + size_t(b) * (64 * kTcRowBytes), &tmap_w2,
+                                 t * TN + crank * PS::kPN + b * 64, kc * 64, full0, keep);
         }
       // the MMAs that read the last stages have completed, and their commits
       // to this CTA have arrived
@@ -1144,11 +1154,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
       uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
       int q = 0;
       for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb)
-        for (int c = 0; c < kWChunks; ++c, ++q) {
+        for (int c = 0; c < NCH; ++c, ++q) {
           const int s = q % kWStagesU;
           if (!mbar_wait_parity(&bar_uempty[g][s], ((q / kWStagesU) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
           mbar_arrive_expect_tx(&bar_ufull[g][s], uint32_t(kWStageU));
-          tc::tma_load_3d_hint(ring + size_t(s) * kWStageU, &tmap_u, t * kWN + c * 64, a.k - 1, row0,
+          tc::tma_load_3d_hint(ring + size_t(s) * kWStageU, &tmap_u, t * TN + c * 64, a.k - 1, row0,
                                &bar_ufull[g][s], once);
         }
       for (int d = (q >= kWStagesU ? q - kWStagesU : 0); d < q; ++d)
@@ -1162,21 +1172,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int q = 0, i = 0;
       bool ok = true;
       for (int t = j0; t < nwt && ok; t += ta.per_mb, ++i) {
-        const int tb = i & 1;
-        if (!mbar_wait_parity(&bar_tempty[tb], ((i >> 1) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
+        const int tb = i % NACC;                   // accumulator
+        if (!mbar_wait_parity(&bar_tempty[tb], ((i / NACC) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; break; }
         tc::fence_after_sync();
-        const uint32_t dtm = tmem + uint32_t(tb * kWN);
+        const uint32_t dtm = tmem + uint32_t(tb * TN);
         for (int kc = 0; kc < ta.nkc; ++kc, ++q) {
           const int s = q % NS;
           if (!mbar_wait_parity(&bar_full[s], (q / NS) & 1, kTcMaxPolls)) { s_err = 1; ok = false; break; }
           tc::fence_after_sync();
-          const uint64_t dbs = db0 + uint64_t(s) * (kPStageB / 16);
+          const uint64_t dbs = db0 + uint64_t(s) * (PS::kStageB / 16);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // A: chunk kc (16 KB apart), 32-byte K step; B: 16 k-rows = two 1024-byte groups
             const uint64_t da = da0 + uint64_t(kc * (kTcBM * kTcRowBytes / 16) + kk * 2);
             const uint64_t db = dbs + uint64_t(kk * (2048 / 16));
-            tc::mma_bf16_pair(dtm, da, db, kPIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16_pair(dtm, da, db, PS::kIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
           }
           tc::commit_pair(&bar_empty[s], 0x3);    // both CTAs' stage s is free once these MMAs have read it
         }
@@ -1185,39 +1195,40 @@ __global__ void __launch_bounds__(kWThreads, 1)
       tc::commit_pair(&bar_done, 0x1);
       if (!mbar_wait_parity(&bar_done, 0, kTcMaxPolls)) s_err = 1;
       // both CTAs' epilogues have released the accumulators of the last tiles
-      for (int tb = 0; tb < 2; ++tb) {
-        const int uses = (i + 1 - tb) / 2;
+      for (int tb = 0; tb < NACC; ++tb) {
+        const int uses = (i + NACC - 1 - tb) / NACC;   // tiles 0 .. i-1 with index % NACC == tb
         if (uses > 0 && !mbar_wait_parity(&bar_tempty[tb], (uses - 1) & 1, kTcMaxPolls)) s_err = 1;
       }
     }
   } else {
-    // ---- epilogue group g = warp / 4 takes tiles i = g, g + 2, ...; thread = request row
+    // ---- epilogue group g = warp / 4 takes tiles i = g, g + 2, ... (accumulator
+    // i % NACC); thread = request row
     const int g = warp >> 2, qd = warp & 3;
     const int rl = qd * 32 + lane;
     const int r = row0 + rl;
     const bool rv = r < a.R;
     const uint64_t keep_part = tc::policy_evict_last();
-    const uint32_t tempty0 = cluster_map_shared(&bar_tempty[g], 0);
     uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
     int i = g;
     for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb, i += 2) {
-      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[g], (i >> 1) & 1, kTcMaxPolls))) {
+      const int tb = i % NACC;
+      if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_tfull[tb], (i / NACC) & 1, kTcMaxPolls))) {
         s_err = 1;
         break;
       }
       tc::fence_after_sync();
       bool ok = true;
-      for (int c = 0; c < kWChunks; ++c) {
-        const int q = (i >> 1) * kWChunks + c, us = q % kWStagesU;   // this group's chunk sequence
+      for (int c = 0; c < NCH; ++c) {
+        const int q = (i >> 1) * NCH + c, us = q % kWStagesU;   // this group's chunk sequence
         float acc0[32], acc1[32];
-        const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(g * kWN + c * 64);
+        const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(tb * TN + c * 64);
         tc::tmem_ld32(taddr, acc0);
         tc::tmem_ld32(taddr + 32, acc1);
         tc::tmem_ld_wait();
-        if (c == kWChunks - 1) {               // this CTA's half of the accumulator has been read
+        if (c == NCH - 1) {                    // this CTA's half of the accumulator has been read
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty0);
+          if (lane == 0) mbar_arrive_cluster(cluster_map_shared(&bar_tempty[tb], 0));
         }
         if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_ufull[g][us], (q / kWStagesU) & 1, kTcMaxPolls))) {
           s_err = 1;
@@ -1228,7 +1239,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         const uint8_t* urow = ring + size_t(us) * kWStageU;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) u[cc] = *reinterpret_cast<const uint4*>(urow + sw128(rl, cc));
-        const int n0 = t * kWN + c * 64;
+        const int n0 = t * TN + c * 64;
         float L[64];
         chunk_logits(u, acc0, acc1, a.logits_bf16, L);
         // The U slot is released once the adds above have consumed every value
@@ -1601,6 +1612,8 @@ int sm_count() {
   return n;
 }
 
+constexpr int kPairTN = 256;      // markov_tc2 tile width (128: four accumulators, measured slower)
+
 // Clusters of two CTAs of `fn` (one CTA per SM) that can be resident at once;
 // 0 on failure.  Cached per device.
 int pair_clusters(const void* fn, size_t smem_bytes) {
@@ -1730,7 +1743,7 @@ extern "C" specv_status specv_markov_draft(const void* U, const void* W1, const 
     void* tc_fn;
     size_t tc_bytes;
     if (pair) {
-      tc_fn = reinterpret_cast<void*>(&markov_tc2_kernel);
+      tc_fn = reinterpret_cast<void*>(&markov_tc2_kernel<kPairTN>);
       tc_bytes = kPSmem;
     } else {
       tc_fn = wide ? reinterpret_cast<void*>(&markov_tcw_kernel) : reinterpret_cast<void*>(&markov_tc_kernel<2>);
