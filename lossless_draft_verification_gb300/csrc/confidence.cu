@@ -7,9 +7,9 @@
 //   c_{r,k} = sigmoid(w_h . h_{r,k} + w_e . W1[x_{r,k-1}] + b),  x_{r,0} = anchor.
 // The scheduler consumes every c_k after the draft is complete, so all
 // positions are computed at once, one warp per (request, position): 16-byte
-// loads of the bf16 rows of h and W1 (each read once: HBM-bound), float32 FMAs
-// against the float32 weights (shared by every warp, so L1/L2-resident), a
-// warp sum and the sigmoid.
+// loads of the bf16 rows of h and W1 (each read once: HBM-bound), eight per lane
+// in flight before their FMAs, against the float32 weights, which each CTA
+// first copies into shared memory; then a warp sum and the sigmoid.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -20,6 +20,7 @@
 namespace specv {
 
 constexpr int kConfWarps = 8;
+constexpr int kConfSmemMaxW = 24 * 1024;    // weights (H + rank floats) staged in shared memory up to this count
 
 struct ConfArgs {
   const uint16_t* h;          // [R, gamma, H] bf16
@@ -32,7 +33,47 @@ struct ConfArgs {
   float b;
   int R, gamma, H, V, rank;
   int vec;                    // 16-byte vectors (rows aligned, H and rank multiples of 8)
+  int smem_w;                 // vec and H + rank <= kConfSmemMaxW: weights read from shared memory
 };
+
+// The same sum with the weights in shared memory: each lane's loads of x for
+// eight consecutive steps are issued before their FMAs.  The FMA order per lane
+// is the one of dot_bf16 (steps i = lane * 8 + 256 j in increasing j, even
+// elements into acc, odd into acc2), so the two give identical results.
+// eight bf16 values of x at element i against the staged weights
+__device__ __forceinline__ void fma8_sw(uint4 v, const float* sw, int i, float& acc, float& acc2) {
+  const float4 w0 = *reinterpret_cast<const float4*>(sw + i);
+  const float4 w1 = *reinterpret_cast<const float4*>(sw + i + 4);
+  acc = fmaf(__uint_as_float(v.x << 16), w0.x, acc);
+  acc2 = fmaf(__uint_as_float(v.x & 0xFFFF0000u), w0.y, acc2);
+  acc = fmaf(__uint_as_float(v.y << 16), w0.z, acc);
+  acc2 = fmaf(__uint_as_float(v.y & 0xFFFF0000u), w0.w, acc2);
+  acc = fmaf(__uint_as_float(v.z << 16), w1.x, acc);
+  acc2 = fmaf(__uint_as_float(v.z & 0xFFFF0000u), w1.y, acc2);
+  acc = fmaf(__uint_as_float(v.w << 16), w1.z, acc);
+  acc2 = fmaf(__uint_as_float(v.w & 0xFFFF0000u), w1.w, acc2);
+}
+
+// Steps i = i_start, i_start + 256, ... < n of the lane-strided sum with the
+// weights in shared memory, eight loads in flight before their FMAs, continuing
+// acc / acc2 (from i_start = lane * 8 the FMA order per lane is dot_bf16's:
+// even elements into acc, odd into acc2, so the two give identical results)
+__device__ __forceinline__ void dot_bf16_sw(const uint16_t* x, const float* sw, int n, int i_start, float& acc,
+                                            float& acc2) {
+  for (int i0 = i_start; i0 < n; i0 += 32 * 8 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 * 8;
+      v[u] = i < n ? ldg_stream(x + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * 32 * 8;
+      if (i < n) fma8_sw(v[u], sw, i, acc, acc2);
+    }
+  }
+}
 
 // sum_i bf16(x[i]) * w[i] over n elements, lane-strided; float32 FMAs
 __device__ __forceinline__ float dot_bf16(const uint16_t* x, const float* w, int n, bool vec, int lane) {
@@ -62,15 +103,34 @@ __device__ __forceinline__ float dot_bf16(const uint16_t* x, const float* w, int
 }
 
 __global__ void __launch_bounds__(kConfWarps * 32) confidence_kernel(ConfArgs a) {
+  extern __shared__ __align__(16) float s_w[];   // [H + rank] when smem_w
   if (blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.smem_w) {
+    const int nw = a.H + a.rank;                 // a multiple of 8
+    for (int i = threadIdx.x * 4; i < nw; i += kConfWarps * 32 * 4)
+      *reinterpret_cast<float4*>(s_w + i) = __ldg(reinterpret_cast<const float4*>(a.w + i));
+    __syncthreads();
+  }
   const long item = long(blockIdx.x) * kConfWarps + warp;
   if (item >= long(a.R) * a.gamma) return;
   const int r = int(item / a.gamma), k = int(item - long(r) * a.gamma);
   const int x = k == 0 ? __ldg(a.anchor + r) : __ldg(a.tokens + size_t(r) * a.gamma + k - 1);
   const bool bad = x < 0 || x >= a.V;
-  float z = dot_bf16(a.h + size_t(item) * a.H, a.w, a.H, a.vec != 0, lane);
-  if (!bad) z += dot_bf16(a.W1 + size_t(x) * a.rank, a.w + a.H, a.rank, a.vec != 0, lane);
+  float z;
+  if (a.smem_w) {
+    float acc = 0.f, acc2 = 0.f;
+    dot_bf16_sw(a.h + size_t(item) * a.H, s_w, a.H, lane * 8, acc, acc2);
+    z = acc + acc2;
+    if (!bad) {
+      float e = 0.f, e2 = 0.f;
+      dot_bf16_sw(a.W1 + size_t(x) * a.rank, s_w + a.H, a.rank, lane * 8, e, e2);
+      z += e + e2;
+    }
+  } else {
+    z = dot_bf16(a.h + size_t(item) * a.H, a.w, a.H, a.vec != 0, lane);
+    if (!bad) z += dot_bf16(a.W1 + size_t(x) * a.rank, a.w + a.H, a.rank, a.vec != 0, lane);
+  }
   z = warp_sum(z);
   if (lane == 0) {
     // sigmoid(z + b) = 1 / (1 + 2^(-(z + b) * log2 e)); saturates to 0 and 1
@@ -119,10 +179,16 @@ extern "C" specv_status specv_confidence_head(const void* h, const void* W1, con
   ca.V = V;
   ca.rank = rank;
   ca.vec = (H % 8 == 0 && rank % 8 == 0 && aligned_to(h, 16) && aligned_to(W1, 16) && aligned_to(w, 16)) ? 1 : 0;
+  ca.smem_w = (ca.vec && H + rank <= kConfSmemMaxW) ? 1 : 0;
+  const size_t smem = ca.smem_w ? size_t(H + rank) * sizeof(float) : 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(reinterpret_cast<const void*>(&confidence_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem)) != cudaSuccess)
+    return SPECV_ERR_CUDA;
   const long items = long(R) * gamma;
   const unsigned grid = unsigned((items + kConfWarps - 1) / kConfWarps);
   void* args[] = {&ca};
-  if (cudaLaunchKernel(reinterpret_cast<const void*>(&confidence_kernel), dim3(grid), dim3(kConfWarps * 32), args, 0,
+  if (cudaLaunchKernel(reinterpret_cast<const void*>(&confidence_kernel), dim3(grid), dim3(kConfWarps * 32), args, smem,
                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPECV_ERR_CUDA;
   return SPECV_OK;

@@ -60,15 +60,24 @@ template <int EPT>
 __device__ __forceinline__ void build_pool(const float* conf, int R, int gamma, int n, int n_pad,
                                            unsigned long long* key, int* idx, long long* pre, int* idx2, int* s_bad) {
   const int tid = threadIdx.x;
-  // survival products, one request per thread
+  // survival products, one request per thread; the confidences are loaded
+  // eight at a time before they are used
   for (int r = tid; r < R; r += kSchedThreads) {
     double prod = 1.0;
-    for (int j = 0; j < gamma; ++j) {
-      const float c = conf[size_t(r) * gamma + j];
-      if (!(c >= 0.f && c <= 1.f)) *s_bad = 1;
-      prod = __dmul_rn(prod, double(c));
-      key[r * gamma + j] = ~static_cast<unsigned long long>(__double_as_longlong(prod));
-      idx[r * gamma + j] = r * gamma + j;
+    for (int j0 = 0; j0 < gamma; j0 += 8) {
+      float cj[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) cj[u] = j0 + u < gamma ? __ldg(conf + size_t(r) * gamma + j0 + u) : 1.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        if (j >= gamma) break;
+        const float c = cj[u];
+        if (!(c >= 0.f && c <= 1.f)) *s_bad = 1;
+        prod = __dmul_rn(prod, double(c));
+        key[r * gamma + j] = ~static_cast<unsigned long long>(__double_as_longlong(prod));
+        idx[r * gamma + j] = r * gamma + j;
+      }
     }
   }
   for (int i = n + tid; i < n_pad; i += kSchedThreads) {
@@ -212,11 +221,18 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedArgs a)
   int taken = 0;
   double theta_taken = 0.0;
   if (!a.global) {
-    // early stop: the first m >= 1 whose Theta does not rise
+    // early stop: the first m >= 1 whose Theta does not rise (each thread's
+    // first stop in its strided m, then one shared atomic per warp)
+    int first = n + 1;
     for (int m = 1 + tid; m <= n; m += kSchedThreads) {
       const bool stop = R + m > a.B_max || !(th[m - 1] > (m > 1 ? th[m - 2] : theta0));
-      if (stop) atomicMin(&s_first, m);
+      if (stop) {
+        first = m;
+        break;
+      }
     }
+    first = int(__reduce_min_sync(0xffffffffu, unsigned(first)));
+    if (lane == 0 && first <= n) atomicMin(&s_first, first);
     __syncthreads();
     taken = s_first - 1;
     theta_taken = theta(taken);
