@@ -232,6 +232,17 @@ def test_markov_tokens_only(lib, T):
     assert differ <= 3 + 900 // 50
 
 
+@pytest.mark.parametrize("R,V,rank,T", [(130, 4104, 128, 1.0), (130, 4104, 128, 0.0), (257, 1000, 64, 1.0)])
+def test_markov_tokens_only_pair_shapes(lib, R, V, rank, T):
+    """CTA-pair drafting (more than one 128-request block, no logits kept) at
+    ragged shapes: a second block of 2 rows (R = 130) or an empty fourth block
+    (R = 257), a last 256-column tile that is almost all past V (one CTA's half
+    entirely), rank 128 and 64, T = 1 and T = 0."""
+    m = synth.markov(seed=309, R=R, gamma=3, V=V, rank=rank, temperature=T, w_scale=0.3)
+    _, differ = _markov_tokens_only_check(lib, m, T)
+    assert differ <= 3 + R * 3 // 50
+
+
 def test_markov_tokens_only_dspark_shape(lib):
     """R=512, gamma=7, V=129280, rank 256 with no logits kept (the drafting step
     of a DSpark round whose verification recomputes the draft logits)."""
