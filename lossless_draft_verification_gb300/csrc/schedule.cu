@@ -8,9 +8,9 @@
 // taken entries of each request form a prefix and l_r is their count.
 //
 // Parallel form: survival products (float64, left to right, one thread per
-// request), a merge sort of (a, index) pairs that starts from the requests'
-// own runs (already ordered) -- ceil(log2 R) merge-path levels in shared
-// memory -- then a block-wide
+// request), a sort of (a, index) pairs -- each warp sorts a chunk in registers
+// by a bitonic network, then merge-path levels in shared memory join the
+// chunks -- then a block-wide
 // int64 prefix sum of the fixed-point increments floor(a * 2^48) (exact, so
 // identical to any sequential order), Theta_n for every n at once, and a
 // block minimum over the first descent.
@@ -86,20 +86,75 @@ __device__ __forceinline__ void build_pool(const float* conf, int R, int gamma, 
   }
   __syncthreads();
 
-  // Sort (key, idx) ascending by merging runs.  A request's products do not
-  // increase with j (each factor is at most 1 and rounding is monotone), so
-  // [r*gamma, r*gamma + gamma) is already an ascending run, and the keys are
-  // distinct pairs (idx breaks ties): merging adjacent runs level by level
-  // gives the one sorted order.  Merge path: each thread writes EPT
-  // consecutive outputs, locating its first one (and the first one of a new
-  // block) by binary search over the two runs; the second buffer is the
-  // prefix array, unused until the sort is done.
+  // Sort (key, idx) ascending; the pairs are distinct (idx breaks ties), so
+  // there is one sorted order.  First each warp sorts its chunk of 32 * EPT
+  // pairs in registers with a bitonic network (lane l holds chunk elements
+  // l * EPT .. l * EPT + EPT - 1; partners at distance >= EPT are in another
+  // lane and come by shuffle), then the chunks are merged level by level.
+  {
+    constexpr int CH = 32 * EPT;
+    const int lane = tid & 31;
+    const int base = (tid >> 5) * CH + lane * EPT;
+    unsigned long long k[EPT];
+    int ix[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      k[e] = key[base + e];
+      ix[e] = idx[base + e];
+    }
+#pragma unroll
+    for (int kk = 2; kk <= CH; kk <<= 1) {
+#pragma unroll
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        if (j >= EPT) {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            const int pos = lane * EPT + e;
+            const bool up = (pos & kk) == 0, lower = (pos & j) == 0;
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, k[e], j / EPT);
+            const int oi = __shfl_xor_sync(0xffffffffu, ix[e], j / EPT);
+            // the lower position of an ascending pair keeps the smaller pair, etc.
+            if ((lower == up) == pair_less(ok, oi, k[e], ix[e])) {
+              k[e] = ok;
+              ix[e] = oi;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            if (e & j) continue;
+            const int f = e | j;
+            const bool up = ((lane * EPT + e) & kk) == 0;
+            const bool swap = up ? pair_less(k[f], ix[f], k[e], ix[e]) : pair_less(k[e], ix[e], k[f], ix[f]);
+            if (swap) {
+              const unsigned long long tk = k[e];
+              const int ti = ix[e];
+              k[e] = k[f];
+              ix[e] = ix[f];
+              k[f] = tk;
+              ix[f] = ti;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      key[base + e] = k[e];
+      idx[base + e] = ix[e];
+    }
+  }
+  __syncthreads();
+
+  // Merge path: each thread writes EPT consecutive outputs, locating its first
+  // one (and the first one of a new block) by binary search over the two runs;
+  // the second buffer is the prefix array, unused until the sort is done.
   {
     unsigned long long* kin = key;
     int* iin = idx;
     unsigned long long* kout = reinterpret_cast<unsigned long long*>(pre);
     int* iout = idx2;
-    for (int len = gamma; len > 0 && len < n; len <<= 1) {
+    for (int len = 32 * EPT; len < n; len <<= 1) {
       const int p0 = tid * EPT;
       int a0 = 0, la = 0, lb = 0, i = 0, j = 0, blk_end = -1;
       for (int p = p0; p < p0 + EPT && p < n; ++p) {
