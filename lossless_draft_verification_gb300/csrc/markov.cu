@@ -288,9 +288,6 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
   __shared__ int s_sel;
   __shared__ float s_base, s_target;
   __shared__ MarkovPart s_part[kSampleMaxPer * kSampleThreads * 9 / 8];   // tile t at t + t / 8
-  // The next step's grid may be scheduled now (it sets up and then waits, in
-  // griddepcontrol.wait, for this grid to complete).
-  pdl_launch_dependents();
   pdl_wait_primary();                      // the logits and partials of this step are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x;
@@ -333,6 +330,7 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
         a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad_in ? -1 : i;
         if (bad_in) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
       }
+      pdl_launch_dependents();
     }
     return;
   }
@@ -465,7 +463,7 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
     }
     __syncthreads();
   }
-  if (warp != 0) return;                   // warp 0 rescans the selected tile and writes the token
+  if (warp != 0) return;                   // warp 0 triggers the next step once the token is written
   if (!bad) {
     // rescan the selected tile's columns in index order
     const MarkovPart p = part[sel];
@@ -509,6 +507,7 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
     a.tokens[size_t(r) * a.gamma + (a.k - 1)] = bad ? -1 : tok;
     if (bad) record_device_error(a.workspace, SPECV_ERR_DEVICE_DATA);
   }
+  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -597,9 +596,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 1) tc::tmem_alloc(&s_tmem, kTcTmemCols);
-  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
-  // for this grid to complete.
-  pdl_launch_dependents();
   pdl_wait_primary();                      // the previous step's tokens are complete
   // the error word is reset once per call, after the work before it completes
   if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
@@ -769,6 +765,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tmem_dealloc(tmem, kTcTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+  pdl_launch_dependents();   // measured: triggering at the start instead was slower
 }
 
 // ---------------------------------------------------------------------------
@@ -837,9 +834,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 3) tc::tmem_alloc(&s_tmem, kWTmemCols);
-  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
-  // for this grid to complete.
-  pdl_launch_dependents();
   pdl_wait_primary();                      // the previous step's tokens are complete
   // the error word is reset once per call, after the work before it completes
   if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
@@ -1021,6 +1015,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     tc::tmem_dealloc(tmem, kWTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+  pdl_launch_dependents();   // measured: triggering at the start instead was slower
 }
 
 // ---------------------------------------------------------------------------
@@ -1098,9 +1093,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
     fence_mbar_init();
   }
   if (warp == kTcEpiWarps + 3) tc::tmem_alloc_pair(&s_tmem, kWTmemCols);
-  // The sampler's grid may be scheduled now; it waits in griddepcontrol.wait
-  // for this grid to complete.
-  pdl_launch_dependents();
   pdl_wait_primary();                      // the previous step's tokens are complete
   // the error word is reset once per call, after the work before it completes
   if (a.k == 1 && blockIdx.x == 0 && threadIdx.x == 0) *reinterpret_cast<int*>(a.workspace) = 0;
@@ -1265,6 +1257,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     tc::tmem_dealloc_pair(tmem, kWTmemCols);
   }
   if (threadIdx.x == 0 && s_err) record_device_error(a.workspace, SPECV_ERR_TIMEOUT);
+  pdl_launch_dependents();   // measured: triggering at the start instead was slower
 }
 
 // ---------------------------------------------------------------------------
