@@ -428,10 +428,12 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
     // No logits were kept (tensor-core form, tile_w = 64): recompute the
     // selected tile's 64 logits, L(v) = U_k(v) + sum_j W1[x_{k-1}, j] W2[j, v].
     // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
-    // 4-byte load per row, all independent; the warps' float32 sums are then
+    // 4-byte load per row, all independent, sixteen issued at a time (eight and
+    // all thirty-two were measured slower); the warps' float32 sums are then
     // added in warp order.
     // Warp w takes rank rows 32w .. 32w + 31 and lane l columns 2l, 2l + 1: one
-    // 4-byte load per row, all independent; the warps' float32 sums are then
+    // 4-byte load per row, all independent, sixteen issued at a time (eight and
+    // all thirty-two were measured slower); the warps' float32 sums are then
     // added in warp order.
     const int v2 = sel * 64 + 2 * lane;                  // this lane's column pair (s_e was filled at the start)
     const int per_w = (a.rank + kSampleWarps - 1) / kSampleWarps;
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(kSampleThreads, 4) markov_sample_kernel(Markov
     if (!bad && v2 < a.V) {
       const int j0 = warp * per_w, j1 = min(a.rank, j0 + per_w);
       const uint16_t* w2 = a.W2 + v2;
-#pragma unroll 8
+#pragma unroll 16
       for (int j = j0; j < j1; ++j) {
         const uint32_t pr = *reinterpret_cast<const uint32_t*>(w2 + size_t(j) * a.V);   // V even: 4-byte aligned
         acc = fma2(make_float2(s_e[j], s_e[j]), make_float2(__uint_as_float(pr << 16), __uint_as_float(pr & 0xFFFF0000u)),
