@@ -989,22 +989,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
             if (lane == 0) {
               tc::tma_store_3d(&tmap_l, n0, ta.lz, z, wst);
               tc::bulk_commit();
-              tc::bulk_wait_read_all();
             }
           }
         }
-        // The slot is released only now: the adds above consumed every value
-        // read from it (and a store has read what was staged in it), so no read
-        // can still be outstanding when the copy of a later chunk overwrites it.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_uempty[g][us]);
         if (n0 + 64 > a.V) {
 #pragma unroll
           for (int j = 0; j < 64; ++j)
             if (n0 + j >= a.V) L[j] = neg_inf();
         }
-        if (!rv || n0 >= a.V) continue;
-        store_part(a.part + size_t(r) * a.ntile + (n0 >> 6), chunk_partial(L, n0, a), keep_part);
+        MarkovPart mp;
+        const bool wp = rv && n0 < a.V;
+        if (wp) mp = chunk_partial(L, n0, a);
+        // The slot is released only now: the adds above consumed every value
+        // read from it, and the store has read what was staged in it (waited
+        // for after the partial, which overlaps the store's read), so no read
+        // can still be outstanding when the copy of a later chunk overwrites it.
+        if (a.logits != nullptr && lane == 0) tc::bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_uempty[g][us]);
+        if (wp) store_part(a.part + size_t(r) * a.ntile + (n0 >> 6), mp, keep_part);
       }
       if (!ok) break;
     }
@@ -1040,17 +1043,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
 // precedes exit, so no copy or arrival targets a CTA that has exited.
 // TN: columns per tile (the MMA's N).  The tensor memory's 512 columns hold
 // 512 / TN accumulators; each CTA stages TN / 2 W2 columns per rank chunk in a
-// ring of 96 KB.
+// ring of 64 KB.
 template <int TN>
 struct PairShape {
   static constexpr int kChunks = TN / 64;                               // 64-column chunks per tile
   static constexpr int kAcc = 512 / TN;                                 // accumulators
   static constexpr int kPN = TN / 2;                                    // W2 columns per CTA per tile
   static constexpr size_t kStageB = size_t(kPN / 64) * 64 * kTcRowBytes;   // one rank chunk of them
-  static constexpr int kStages = int(96 * 1024 / kStageB);
+  static constexpr int kStages = int(64 * 1024 / kStageB);
   static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(2 * kTcBM, TN, true);   // M = 256 over the pair, B MN-major
 };
-constexpr size_t kPSmem = kTcSmemE + 96 * 1024 + 2 * kWStagesU * kWStageU + 1024;
+constexpr int kPStagesU = 3;     // U chunks in flight per epilogue group (the epilogue sets the pace)
+constexpr size_t kPSmem = kTcSmemE + 64 * 1024 + 2 * kPStagesU * kWStageU + 1024;
 
 template <int TN>
 __global__ void __launch_bounds__(kWThreads, 1)
@@ -1060,7 +1064,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   constexpr int NS = PS::kStages, NACC = PS::kAcc, NCH = PS::kChunks;
   const MarkovArgs& a = ta.m;
   extern __shared__ uint8_t s_raw[];
-  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_ufull[2][kWStagesU], bar_uempty[2][kWStagesU],
+  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS], bar_ufull[2][kPStagesU], bar_uempty[2][kPStagesU],
       bar_tfull[NACC], bar_tempty[NACC], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_err;
@@ -1082,7 +1086,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_init(&bar_empty[i], 1);
     }
     for (int g = 0; g < 2; ++g)
-      for (int i = 0; i < kWStagesU; ++i) {
+      for (int i = 0; i < kPStagesU; ++i) {
         mbar_init(&bar_ufull[g][i], 1);
         mbar_init(&bar_uempty[g][i], 4);
       }
@@ -1145,18 +1149,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int g = warp - (kTcEpiWarps + 1);
     if (lane == 0) {
       const uint64_t once = tc::policy_evict_first();
-      uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+      uint8_t* ring = sU + size_t(g) * kPStagesU * kWStageU;
       int q = 0;
       for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb)
         for (int c = 0; c < NCH; ++c, ++q) {
-          const int s = q % kWStagesU;
-          if (!mbar_wait_parity(&bar_uempty[g][s], ((q / kWStagesU) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
+          const int s = q % kPStagesU;
+          if (!mbar_wait_parity(&bar_uempty[g][s], ((q / kPStagesU) & 1) ^ 1, kTcMaxPolls)) { s_err = 1; t = nwt; break; }
           mbar_arrive_expect_tx(&bar_ufull[g][s], uint32_t(kWStageU));
           tc::tma_load_3d_hint(ring + size_t(s) * kWStageU, &tmap_u, t * TN + c * 64, a.k - 1, row0,
                                &bar_ufull[g][s], once);
         }
-      for (int d = (q >= kWStagesU ? q - kWStagesU : 0); d < q; ++d)
-        if (!mbar_wait_parity(&bar_ufull[g][d % kWStagesU], (d / kWStagesU) & 1, kTcMaxPolls)) s_err = 1;
+      for (int d = (q >= kPStagesU ? q - kPStagesU : 0); d < q; ++d)
+        if (!mbar_wait_parity(&bar_ufull[g][d % kPStagesU], (d / kPStagesU) & 1, kTcMaxPolls)) s_err = 1;
     }
   } else if (warp == kTcEpiWarps + 3) {
     // ---- pair MMA issuer (even CTA)
@@ -1202,7 +1206,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int r = row0 + rl;
     const bool rv = r < a.R;
     const uint64_t keep_part = tc::policy_evict_last();
-    uint8_t* ring = sU + size_t(g) * kWStagesU * kWStageU;
+    uint8_t* ring = sU + size_t(g) * kPStagesU * kWStageU;
     int i = g;
     for (int t = j0 + g * ta.per_mb; t < nwt; t += 2 * ta.per_mb, i += 2) {
       const int tb = i % NACC;
@@ -1213,7 +1217,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       tc::fence_after_sync();
       bool ok = true;
       for (int c = 0; c < NCH; ++c) {
-        const int q = (i >> 1) * NCH + c, us = q % kWStagesU;   // this group's chunk sequence
+        const int q = (i >> 1) * NCH + c, us = q % kPStagesU;   // this group's chunk sequence
         float acc0[32], acc1[32];
         const uint32_t taddr = tmem + (uint32_t(qd * 32) << 16) + uint32_t(tb * TN + c * 64);
         tc::tmem_ld32(taddr, acc0);
@@ -1224,7 +1228,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(cluster_map_shared(&bar_tempty[tb], 0));
         }
-        if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_ufull[g][us], (q / kWStagesU) & 1, kTcMaxPolls))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_parity(&bar_ufull[g][us], (q / kPStagesU) & 1, kTcMaxPolls))) {
           s_err = 1;
           ok = false;
           break;
