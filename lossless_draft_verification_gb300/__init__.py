@@ -293,6 +293,18 @@ def _raise(status, where):
         raise SpecvError(status, where)
 
 
+_copy_streams = {}
+
+
+def _copy_streams_for(dev):
+    """Two copy streams per device, created once (stream creation is not free)."""
+    torch = _torch()
+    key = dev.index
+    if key not in _copy_streams:
+        _copy_streams[key] = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    return _copy_streams[key]
+
+
 def _verify_chain_host_chunked(target, draft, draft_tokens, uniforms, temperature, lengths, want_c_star, chunks,
                                stream):
     """Host inputs, requests split into `chunks` groups: group i's host-to-device
@@ -310,11 +322,12 @@ def _verify_chain_host_chunked(target, draft, draft_tokens, uniforms, temperatur
     d_x = torch.empty(draft_tokens.shape, dtype=draft_tokens.dtype, device=dev)
     d_u = None if uniforms is None else torch.empty(uniforms.shape, dtype=uniforms.dtype, device=dev)
     d_l = None if lengths is None else torch.empty(lengths.shape, dtype=lengths.dtype, device=dev)
-    acc = torch.empty(R, dtype=torch.int32, device=dev)
-    tok = torch.empty(R, dtype=torch.int32, device=dev)
-    cst = torch.empty(R, gamma, dtype=torch.float32, device=dev) if want_c_star else None
+    # the three outputs share one device buffer, so one transfer returns them
+    out = torch.empty(2 * R + (R * gamma if want_c_star else 0), dtype=torch.int32, device=dev)
+    acc, tok = out[:R], out[R:2 * R]
+    cst = out[2 * R:].view(torch.float32).view(R, gamma) if want_c_star else None
     code = _dtype_code(target)
-    copies = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    copies = _copy_streams_for(dev)
     for c in copies:
         c.wait_stream(comp)                 # the device buffers were allocated on the compute stream
     step = -(-R // chunks)
@@ -345,7 +358,8 @@ def _verify_chain_host_chunked(target, draft, draft_tokens, uniforms, temperatur
             for c in copies:
                 t.record_stream(c)
     with torch.cuda.stream(comp):
-        return acc.cpu(), tok.cpu(), None if cst is None else cst.cpu()
+        h = out.cpu()
+    return h[:R], h[R:2 * R], (h[2 * R:].view(torch.float32).view(R, gamma) if want_c_star else None)
 
 
 def verify_chain(target, draft, draft_tokens, uniforms, temperature: float, lengths=None, want_c_star: bool = True,

@@ -70,6 +70,26 @@ def test_chain_greedy_small(lib, dtype, V):
     _check_greedy(lib, case)
 
 
+@pytest.mark.parametrize("ragged,chunks", [(True, 3), (False, 4)])
+def test_host_inputs_chunked_equal_device_call(lib, ragged, chunks):
+    """Pinned host inputs through verify_chain with `chunks` request groups
+    (copies on two streams overlapping the previous group's kernels, the three
+    outputs returned by one transfer) give exactly the device call's outputs."""
+    import torch
+    case = synth.chain_batched(seed=110, R=10, gamma=4, V=5000, dtype="bf16", ragged_lengths=ragged)
+    A, y, c = _run_chain(lib, case)
+    host = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a.raw.view(np.int16))).view(torch.bfloat16)
+                               if dt is None else torch.from_numpy(np.ascontiguousarray(a.astype(dt)))).pin_memory()
+    h_len = None if case.lengths is None else host(case.lengths, np.int32)
+    for _ in range(2):                            # the second call reuses the cached copy streams
+        Ah, yh, ch = lib.verify_chain(host(case.target), host(case.draft), host(case.tokens, np.int32),
+                                      host(case.uniforms, np.float32), case.temperature, h_len, True, chunks=chunks)
+        assert Ah.device.type == "cpu" and ch.shape == (10, 4)
+        np.testing.assert_array_equal(Ah.numpy(), A)
+        np.testing.assert_array_equal(yh.numpy(), y)
+        np.testing.assert_array_equal(ch.numpy().view(np.int32), c.view(np.int32))   # bitwise, NaN pattern included
+
+
 def test_tiny_chain_config(lib):
     """R=1, gamma=4, V=1024 float32 at T=1 and T=0."""
     for T in (1.0, 0.0):
