@@ -310,9 +310,11 @@ SPECV_API specv_status specv_markov_draft(const void* U, const void* W1, const v
  *   For every request r and k < lengths[r] (all k < gamma when lengths is
  *   NULL): draft_logits[r, k, :] = L (bf16), with x_{k-1} = anchor[r] for
  *   k = 0 and draft_tokens[r, k-1] otherwise.  The sums run on the tensor
- *   cores in the tiling specv_markov_draft uses when it keeps no logits, so
- *   the rows equal the bf16 logits those draws were taken from.  Other rows of
- *   draft_logits are not written.
+ *   cores with the tiling and summation order of specv_markov_draft's
+ *   kept-logits form, so the rows are bitwise the bf16 logits a drafting call
+ *   that keeps them writes; a drafting call that keeps none draws the same
+ *   tokens as one that keeps them except at numerical near-ties of its CDF.
+ *   Other rows of draft_logits are not written.
  *   U [R, gamma, V], W1 [V, rank], W2 [rank, V] bf16; anchor [R],
  *   draft_tokens [R, gamma], lengths [R] int32 (0 <= lengths[r] <= gamma);
  *   draft_logits [R, gamma, V] bf16 out.  Workspace of at least
