@@ -209,12 +209,5 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tmap, in
       : "memory");
 }
 
-// this thread's bulk stores have read their shared-memory sources, except the
-// newest N groups
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 }  // namespace tc
 }  // namespace specv
